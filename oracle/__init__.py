@@ -1,0 +1,195 @@
+"""CPU oracle for EAGLE draft-tree verification — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and
+this package imports nothing from the product.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision); this module
+only marshals numpy arrays into it.  ``build()`` compiles it with gcc.
+
+Parity status of each function (the pins are in ``tests/test_oracle_*.py``):
+  tree_mask         pinned (brute-force ancestor walks over every tree N <= 7,
+                    hand-worked golden fixture)
+  attention         pinned (torch SDPA with an explicit boolean mask, chain ==
+                    sequential causal decode, closed forms, block permutation)
+  accept_greedy     pinned (enumeration of root paths with numpy nanargmax,
+                    golden fixture)
+  accept_stochastic pinned (Philox4x32-10 known-answer vectors, empirical
+                    target-distribution test, degenerate cases, exhaustive
+                    integer-CDF check)
+  kv_compact        pinned (torch index_select + narrow + copy_, the operation
+                    the KVCache.copy passage describes)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, BAD_TREE, OUT_OF_RANGE, UNSUPPORTED, BAD_VALUES = 0, 2, 3, 4, 7
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so (gcc, OpenMP, no fast-math)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = ctypes.CDLL(build())
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+I64 = ctypes.c_int64
+
+
+def tree_mask(parents):
+    """parents int32 [B, N] -> (mask uint64 [B, N], depth int32 [B, N], status int32 [B])."""
+    lib = _load()
+    parents = _c(parents, np.int32)
+    B, N = parents.shape
+    mask = np.zeros((B, N), np.uint64)
+    depth = np.zeros((B, N), np.int32)
+    status = np.zeros(B, np.int32)
+    lib.orc_tree_mask(_p(parents), I64(B), I64(N), _p(mask), _p(depth), _p(status))
+    return mask, depth, status
+
+
+def attention(q, k_cache, v_cache, block_table, prefix_lens, mask, *, bf16: bool,
+              scale: float = 0.0, sel=None, nthreads: int = 1):
+    """Tree-masked paged GQA attention in double precision.
+
+    q: [B, N, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, bs, d]; both float32,
+    or uint16 bfloat16 bit patterns when ``bf16``.  ``sel``: flat node indices
+    b*N+i to evaluate (None: all).  Returns (out float64 [n, Hq, d], status).
+    """
+    lib = _load()
+    dt = np.uint16 if bf16 else np.float32
+    q = _c(q, dt)
+    k_cache = _c(k_cache, dt)
+    v_cache = _c(v_cache, dt)
+    block_table = _c(block_table, np.int32)
+    prefix_lens = _c(prefix_lens, np.int32)
+    mask = _c(mask, np.uint64)
+    B, N, Hq, d = q.shape
+    num_blocks, Hkv, bs, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape
+    sel_arr = None if sel is None else _c(sel, np.int64)
+    n = B * N if sel is None else len(sel_arr)
+    out = np.zeros((n, Hq, d), np.float64)
+    status = np.zeros(B, np.int32)
+    lib.orc_attention(ctypes.c_int(1 if bf16 else 0), _p(q), _p(k_cache), _p(v_cache),
+                      _p(block_table), I64(block_table.shape[1]), _p(prefix_lens), _p(mask),
+                      I64(B), I64(N), I64(Hq), I64(Hkv), I64(d), I64(bs), I64(num_blocks),
+                      ctypes.c_double(scale), _p(sel_arr), I64(0 if sel is None else n),
+                      _p(out), _p(status), ctypes.c_int(nthreads))
+    return out, status
+
+
+def accept_greedy(parents, tokens, logits, max_path):
+    """Greedy acceptance -> (accept_len [B], path [B, max_path], out_tokens, status)."""
+    lib = _load()
+    parents = _c(parents, np.int32)
+    tokens = _c(tokens, np.int32)
+    logits = _c(logits, np.float32)
+    B, N, V = logits.shape
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, max_path), np.int32)
+    out = np.zeros((B, max_path), np.int32)
+    status = np.zeros(B, np.int32)
+    lib.orc_accept_greedy(_p(parents), _p(tokens), _p(logits), I64(B), I64(N), I64(V),
+                          I64(max_path), _p(acc), _p(path), _p(out), _p(status))
+    return acc, path, out, status
+
+
+def accept_stochastic(parents, tokens, p, q, seed, offset, max_path):
+    """Chain rejection sampling -> (accept_len, path, out_tokens, status)."""
+    lib = _load()
+    parents = _c(parents, np.int32)
+    tokens = _c(tokens, np.int32)
+    p = _c(p, np.float32)
+    q = _c(q, np.float32)
+    B, N, V = p.shape
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, max_path), np.int32)
+    out = np.zeros((B, max_path), np.int32)
+    status = np.zeros(B, np.int32)
+    lib.orc_accept_stochastic(_p(parents), _p(tokens), _p(p), _p(q), I64(B), I64(N), I64(V),
+                              ctypes.c_uint64(seed), ctypes.c_uint64(offset), I64(max_path),
+                              _p(acc), _p(path), _p(out), _p(status))
+    return acc, path, out, status
+
+
+def philox4x32_10(counter, key):
+    """One Philox4x32-10 block: counter 4 x uint32, key 2 x uint32 -> 4 x uint32."""
+    lib = _load()
+    c = np.asarray(counter, np.uint32)
+    k = np.asarray(key, np.uint32)
+    o = np.zeros(4, np.uint32)
+    lib.orc_philox4x32_10(_p(c), _p(k), _p(o))
+    return o
+
+
+def sample_weights(w, x):
+    """Integer-CDF sampler: index t with probability w_t / sum(w) for uniform 32-bit x."""
+    lib = _load()
+    w = _c(w, np.uint64)
+    lib.orc_sample_weights_u32.restype = ctypes.c_int64
+    return int(lib.orc_sample_weights_u32(_p(w), I64(len(w)), ctypes.c_uint32(x)))
+
+
+def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, *,
+               num_layers=1, layer_stride=0):
+    """In-place compaction of the numpy caches -> (new_lens, src_slots, dst_slots, status).
+
+    Caches are [num_layers?][num_blocks, Hkv, bs, d] arrays of any 2- or
+    4-byte element type; with num_layers > 1 the caches hold the layers back to
+    back with ``layer_stride`` elements between them.
+    """
+    lib = _load()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    block_table = _c(block_table, np.int32)
+    prefix_lens = _c(prefix_lens, np.int32)
+    path = _c(path, np.int32)
+    accept_len = _c(accept_len, np.int32)
+    num_blocks, Hkv, bs, d = k_cache.shape[-4:]
+    B, max_path = path.shape
+    new_lens = np.zeros(B, np.int32)
+    src = np.zeros((B, max_path), np.int64)
+    dst = np.zeros((B, max_path), np.int64)
+    status = np.zeros(B, np.int32)
+    lib.orc_kv_compact(I64(k_cache.itemsize), _p(k_cache), _p(v_cache), I64(num_layers),
+                       I64(layer_stride), _p(block_table), I64(block_table.shape[1]),
+                       _p(prefix_lens), _p(path), _p(accept_len), I64(max_path), I64(B),
+                       I64(Hkv), I64(d), I64(bs), I64(num_blocks), _p(new_lens), _p(src),
+                       _p(dst), _p(status))
+    return new_lens, src, dst, status
