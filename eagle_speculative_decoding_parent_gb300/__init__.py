@@ -1,0 +1,178 @@
+"""Python binding of libtreeverify (EAGLE draft-tree verification on GB300).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+The functions carry the C entry points' names and take torch CUDA tensors
+(PyTorch is used for device memory and streams).  Each call is asynchronous
+on the current torch stream (or ``stream``) and raises ``TreeVerifyError``
+when the library returns a host-side error; per-sequence data errors are
+reported in the ``status`` tensors, as the C header describes.
+
+There is no CPU fallback: importing this package fails if the compiled
+library is missing (run ``__graft_entry__.build()`` or ``python -m
+eagle_speculative_decoding_parent_gb300._build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTED",
+           "TV_ERR_TIMEOUT", "TV_ERR_BAD_VALUES", "TV_F32", "TV_BF16", "GREEDY", "STOCHASTIC",
+           "TreeVerifyError", "library_path", "status_string", "tree_mask_build",
+           "tree_verify_attention_workspace", "tree_verify_attention", "tree_accept_workspace",
+           "tree_accept", "kv_compact"]
+
+(TV_OK, TV_ERR_INVALID_ARG, TV_ERR_BAD_TREE, TV_ERR_OUT_OF_RANGE, TV_ERR_UNSUPPORTED,
+ TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_ERR_BAD_VALUES, TV_ERR_WORKSPACE) = range(9)
+TV_F32, TV_BF16 = 0, 1
+GREEDY, STOCHASTIC = 0, 1
+
+
+class TreeVerifyError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+if not os.path.exists(_build.LIB):
+    raise ImportError(f"libtreeverify is not built ({_build.LIB} missing); "
+                      "run python -m eagle_speculative_decoding_parent_gb300._build")
+
+_lib = ctypes.CDLL(_build.LIB)
+
+_i, _u64, _i64, _f, _p, _sz = (ctypes.c_int, ctypes.c_uint64, ctypes.c_int64, ctypes.c_float,
+                               ctypes.c_void_p, ctypes.c_size_t)
+
+
+def _sig(name, res, args):
+    fn = getattr(_lib, name)
+    fn.restype = res
+    fn.argtypes = args
+    return fn
+
+
+_status_string = _sig("tv_status_string", ctypes.c_char_p, [_i])
+_abi = _sig("tv_abi_version", _i, [])
+_mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p])
+_attn_ws = _sig("tree_verify_attention_workspace", _sz, [_i, _i, _i, _i, _i, _i, _i, _i])
+_attn = _sig("tree_verify_attention", _i,
+             [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p])
+_acc_ws = _sig("tree_accept_workspace", _sz, [_i, _i, _i, _i])
+_acc = _sig("tree_accept", _i,
+            [_i, _p, _p, _p, _p, _i, _i, _i, _u64, _u64, _p, _p, _p, _i, _p, _p, _sz, _p])
+_compact = _sig("kv_compact", _i,
+                [_p, _p, _i, _i64, _p, _i, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
+                 _p, _p])
+
+assert _abi() == 1, "header / library ABI mismatch"
+
+
+def status_string(code: int) -> str:
+    return _status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != TV_OK:
+        raise TreeVerifyError(f"{what}: {status_string(rc)} ({rc})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("tensors passed to libtreeverify must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libtreeverify must be contiguous")
+    return t.data_ptr()
+
+
+def _want(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return TV_BF16
+    if t.dtype == torch.float32:
+        return TV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def tree_mask_build(parents, mask, depth, status, stream=None) -> None:
+    """parents int32 [B,N] -> mask int64 (uint64 bits) [B,N], depth int32 [B,N] or None, status [B]."""
+    _want(parents, torch.int32, "parents")
+    _want(mask, torch.int64, "mask")
+    B, N = parents.shape
+    _check(_mask(_ptr(parents), B, N, _ptr(mask), _ptr(depth), _ptr(status), _stream(stream)),
+           "tree_mask_build")
+
+
+def tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size,
+                                    dtype=torch.bfloat16) -> int:
+    dt = TV_BF16 if dtype == torch.bfloat16 else TV_F32
+    return int(_attn_ws(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size, dt))
+
+
+def tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, mask, out, status,
+                          workspace=None, *, scale: float = 0.0, stream=None) -> None:
+    """q [B,N,Hq,d]; caches [num_blocks,Hkv,bs,d]; block_table int32 [B,max_blocks];
+    prefix_lens int32 [B]; mask int64 [B,N]; out like q; status int32 [B];
+    workspace uint8 tensor (zero-filled before first use)."""
+    B, N, Hq, d = q.shape
+    num_blocks, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    for t, n in ((block_table, "block_table"), (prefix_lens, "prefix_lens"), (status, "status")):
+        _want(t, torch.int32, n)
+    _want(mask, torch.int64, "mask")
+    dt = _dt(q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                 _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs, num_blocks, dt, scale,
+                 _ptr(out), _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)),
+           "tree_verify_attention")
+
+
+def tree_accept_workspace(mode, B, N, V) -> int:
+    return int(_acc_ws(mode, B, N, V))
+
+
+def tree_accept(mode, parents, draft_tokens, target, draft_probs, accept_len, path, out_tokens,
+                status, *, seed: int = 0, offset: int = 0, workspace=None, stream=None) -> None:
+    """Greedy (target = logits) or stochastic chain (target = p, draft_probs = q) acceptance."""
+    B, N, V = target.shape
+    _want(target, torch.float32, "target")
+    if draft_probs is not None:
+        _want(draft_probs, torch.float32, "draft_probs")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_acc(mode, _ptr(parents), _ptr(draft_tokens), _ptr(target), _ptr(draft_probs), B, N,
+                V, seed, offset, _ptr(accept_len), _ptr(path), _ptr(out_tokens), path.shape[1],
+                _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)), "tree_accept")
+
+
+def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, new_lens, status,
+               *, src_slots=None, dst_slots=None, num_layers: int = 1, layer_stride: int = 0,
+               stream=None) -> None:
+    """Caches [num_layers*][num_blocks,Hkv,bs,d] (layers back to back, ``layer_stride``
+    elements apart); path int32 [B,max_path]; accept_len int32 [B]."""
+    num_blocks, Hkv, bs, d = k_cache.shape[-4:]
+    B, max_path = path.shape
+    _check(_compact(_ptr(k_cache), _ptr(v_cache), num_layers, layer_stride, _ptr(block_table),
+                    block_table.shape[1], _ptr(prefix_lens), _ptr(path), _ptr(accept_len),
+                    max_path, B, Hkv, d, bs, num_blocks, _dt(k_cache), _ptr(new_lens),
+                    _ptr(src_slots), _ptr(dst_slots), _ptr(status), _stream(stream)),
+           "kv_compact")

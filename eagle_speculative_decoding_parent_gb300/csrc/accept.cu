@@ -1,0 +1,497 @@
+// tree_accept: one thread-block cluster per sequence.
+//
+// Each CTA of the cluster owns a contiguous slice of the vocabulary.  Only
+// the rows the acceptance rule needs are read:
+//   greedy      a level-by-level walk from the root: the argmax of every row
+//               on the current frontier of fully matching nodes (usually one)
+//               is reduced inside each CTA, exchanged through distributed
+//               shared memory, and the matching children form the next
+//               frontier; the walk stops at the deepest accepted level, whose
+//               argmax is the bonus token.  Rows read ~ accepted depth + 1.
+//   stochastic  the accept tests touch two scalars per draft; only the row(s)
+//               the emitted token is drawn from are read: integer weights
+//               (exact sums, so the draw does not depend on summation order),
+//               slice sums exchanged across the cluster, and the CTA holding
+//               the target prefix sum scans its slice.
+// All CTAs of a cluster take identical control-flow decisions (they read the
+// same inputs and the same exchanged values), so every cluster barrier is
+// reached by every CTA.
+#include <cooperative_groups.h>
+
+#include "tv_device.cuh"
+#include "tv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace tv {
+
+namespace {
+
+constexpr int ACC_THREADS = 512;
+constexpr int ACC_WARPS = ACC_THREADS / 32;
+constexpr int NO_INDEX = 0x7fffffff;
+
+struct AccParams {
+    const int32_t* parents;
+    const int32_t* tokens;
+    const float* target;
+    const float* draft;
+    int B, N, V;
+    uint64_t seed, offset;
+    int32_t* accept_len;
+    int32_t* path;
+    int32_t* out_tokens;
+    int max_path;
+    int32_t* status;
+};
+
+struct ArgBest {
+    float v;
+    int i;
+};
+
+// (v, i) beats (w, j): larger value, ties to the lower index.  Entries with
+// i == NO_INDEX carry no candidate (v is -inf there).
+__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
+    return (v > w) || (v == w && i < j);
+}
+
+__device__ __forceinline__ void take(ArgBest& a, float x, int i) {
+    if (!isnan(x) && beats(x, i, a.v, a.i)) {
+        a.v = x;
+        a.i = i;
+    }
+}
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), written from the published
+// round function: two 32x32 -> 64-bit products per round, Weyl key schedule.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint4 draw(const AccParams& p, int b, int k) {
+    return philox4x32_10(make_uint4((uint32_t)k, (uint32_t)b, (uint32_t)p.offset,
+                                    (uint32_t)(p.offset >> 32)),
+                         make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
+}
+
+// Fixed-point weight floor(min(x, 1) * 2^40); 0 for NaN and x <= 0.
+__device__ __forceinline__ uint64_t weight(float x) {
+    if (!(x > 0.f)) return 0ull;
+    if (x >= 1.f) return 1ull << 40;
+    return __float2ull_rz(__fmul_rn(x, 1099511627776.f));
+}
+
+__device__ __forceinline__ uint64_t elem_weight(const float* a, const float* bq, int t, bool resid) {
+    return resid ? weight(__fsub_rn(__ldg(a + t), __ldg(bq + t))) : weight(__ldg(a + t));
+}
+
+struct Slice {
+    int lo, hi;      // this CTA's vocabulary range
+    int seg;         // elements per warp segment (multiple of 4)
+};
+
+__device__ __forceinline__ Slice make_slice(int V, int C, int rank) {
+    int per = (V + C - 1) / C;
+    per = (per + 3) & ~3;
+    Slice s;
+    s.lo = min(V, rank * per);
+    s.hi = min(V, s.lo + per);
+    int seg = (s.hi - s.lo + ACC_WARPS - 1) / ACC_WARPS;
+    s.seg = (seg + 3) & ~3;
+    return s;
+}
+
+// Block-wide argmax of row[lo, hi); result valid in every thread.
+template <bool VEC>
+__device__ ArgBest block_argmax(const float* __restrict__ row, int lo, int hi, ArgBest* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    ArgBest a{-INFINITY, NO_INDEX};
+    if (VEC) {
+        const int nv = (hi - lo) >> 2;
+        const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+#pragma unroll 4
+        for (int e = tid; e < nv; e += ACC_THREADS) {
+            const float4 x = __ldg(r4 + e);
+            const int i = lo + 4 * e;
+            take(a, x.x, i);
+            take(a, x.y, i + 1);
+            take(a, x.z, i + 2);
+            take(a, x.w, i + 3);
+        }
+        for (int i = lo + 4 * nv + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
+    } else {
+        for (int i = lo + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, a.v, off);
+        const int j = __shfl_xor_sync(0xffffffffu, a.i, off);
+        if (beats(w, j, a.v, a.i)) {
+            a.v = w;
+            a.i = j;
+        }
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    ArgBest r = red[0];
+    for (int w = 1; w < ACC_WARPS; ++w)
+        if (beats(red[w].v, red[w].i, r.v, r.i)) r = red[w];
+    return r;
+}
+
+// Sum of integer weights over this CTA's slice, per warp segment (kept in
+// wsum[]) and in total.  resid: weight(a - b); otherwise weight(a).
+__device__ uint64_t slice_weight_sum(const float* a, const float* bq, bool resid, const Slice& s,
+                                     uint64_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int slo = min(s.hi, s.lo + warp * s.seg), shi = min(s.hi, slo + s.seg);
+    uint64_t acc = 0;
+    for (int t = slo + lane; t < shi; t += 32) acc += elem_weight(a, bq, t, resid);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    __syncthreads();
+    if (lane == 0) wsum[warp] = acc;
+    __syncthreads();
+    uint64_t tot = 0;
+    for (int w = 0; w < ACC_WARPS; ++w) tot += wsum[w];
+    return tot;
+}
+
+// Within this CTA's slice, the smallest index whose inclusive prefix sum of
+// weights exceeds T (0 <= T < slice sum).  Run by one warp; returns in lane 0.
+__device__ int slice_find(const float* a, const float* bq, bool resid, const Slice& s,
+                          const uint64_t* wsum, uint64_t T) {
+    const int lane = threadIdx.x & 31;
+    int w = 0;
+    while (w < ACC_WARPS - 1 && T >= wsum[w]) {
+        T -= wsum[w];
+        ++w;
+    }
+    const int slo = min(s.hi, s.lo + w * s.seg), shi = min(s.hi, slo + s.seg);
+    for (int base = slo; base < shi; base += 32) {
+        const int t = base + lane;
+        uint64_t x = (t < shi) ? elem_weight(a, bq, t, resid) : 0ull;
+        // inclusive warp scan
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        const uint64_t chunk = __shfl_sync(0xffffffffu, x, 31);
+        if (T < chunk) {
+            const unsigned hit = __ballot_sync(0xffffffffu, x > T);
+            return base + __ffs(hit) - 1;
+        }
+        T -= chunk;
+    }
+    return -1;  // not reached when T < slice sum
+}
+
+__device__ void write_fail(const AccParams& p, int b, int st) {
+    for (int j = threadIdx.x; j < p.max_path; j += blockDim.x) {
+        p.path[(int64_t)b * p.max_path + j] = (j == 0) ? 0 : -1;
+        p.out_tokens[(int64_t)b * p.max_path + j] = -1;
+    }
+    if (threadIdx.x == 0) {
+        p.accept_len[b] = 0;
+        p.status[b] = st;
+    }
+}
+
+// Emits root..chosen and the tokens; rank-0 CTA only (all its threads).
+__device__ void write_path(const AccParams& p, int b, const int* spar, const int* stok,
+                           int chosen, int last) {
+    __shared__ int spath[64];
+    __shared__ int sdep;
+    if (threadIdx.x == 0) {
+        int dep = 0;
+        for (int j = chosen; spar[j] >= 0; j = spar[j]) ++dep;
+        int j = chosen;
+        for (int k = dep; k >= 0; --k) {
+            spath[k] = j;
+            j = spar[j];
+        }
+        sdep = dep;
+    }
+    __syncthreads();
+    const int dep = sdep;
+    if (dep + 1 > p.max_path) {
+        write_fail(p, b, TV_ERR_OUT_OF_RANGE);
+        return;
+    }
+    for (int j = threadIdx.x; j < p.max_path; j += blockDim.x) {
+        p.path[(int64_t)b * p.max_path + j] = (j <= dep) ? spath[j] : -1;
+        int tok = -1;
+        if (j < dep) tok = stok[spath[j + 1]];
+        else if (j == dep) tok = last;
+        p.out_tokens[(int64_t)b * p.max_path + j] = tok;
+    }
+    if (threadIdx.x == 0) {
+        p.accept_len[b] = dep;
+        p.status[b] = TV_OK;
+    }
+}
+
+// Tree and token checks in the order the acceptance rule states them
+// (structure first, then token range).  One thread.
+__device__ int check_inputs(const int* spar, const int* stok, int N, int V, bool chain) {
+    for (int i = 0; i < N; ++i) {
+        const int pa = spar[i];
+        if ((i == 0 && pa != -1) || (i > 0 && (pa < 0 || pa >= i))) return TV_ERR_BAD_TREE;
+    }
+    if (chain)
+        for (int i = 1; i < N; ++i)
+            if (spar[i] != i - 1) return TV_ERR_UNSUPPORTED;
+    for (int i = 1; i < N; ++i)
+        if (stok[i] < 0 || stok[i] >= V) return TV_ERR_OUT_OF_RANGE;
+    return TV_OK;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(ACC_THREADS)
+accept_greedy_kernel(AccParams p) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / C;
+    __shared__ int spar[64], stok[64], sam[64];
+    __shared__ ArgBest exch[2][64];
+    __shared__ ArgBest red[ACC_WARPS];
+    __shared__ int sflag;
+    const int tid = threadIdx.x, N = p.N;
+    if (tid < N) {
+        spar[tid] = p.parents[(int64_t)b * N + tid];
+        stok[tid] = p.tokens[(int64_t)b * N + tid];
+        sam[tid] = -1;
+    }
+    __syncthreads();
+    if (tid == 0) sflag = check_inputs(spar, stok, N, p.V, false);
+    __syncthreads();
+    if (sflag != TV_OK) {
+        if (rank == 0) write_fail(p, b, sflag);
+        return;  // uniform across the cluster: no cluster barrier has been issued
+    }
+    const Slice sl = make_slice(p.V, C, rank);
+    uint64_t frontier = 1ull;  // node 0
+    int par = 0, chosen = 0;
+    // each level is one depth deeper, so the walk ends within N levels
+    for (int level = 0; level < N; ++level) {
+        // local argmax of each frontier row
+        for (uint64_t f = frontier; f; f &= f - 1) {
+            const int u = __ffsll((long long)f) - 1;
+            const float* row = p.target + ((int64_t)b * N + u) * p.V;
+            const ArgBest a = block_argmax<VEC>(row, sl.lo, sl.hi, red);
+            if (tid == 0) exch[par][u] = a;
+        }
+        cluster.sync();
+        // combine across the cluster (thread u handles frontier node u)
+        if (tid < N && ((frontier >> tid) & 1ull)) {
+            ArgBest best{-INFINITY, NO_INDEX};
+            for (int r = 0; r < C; ++r) {
+                const ArgBest* rem = cluster.map_shared_rank(&exch[par][tid], r);
+                const ArgBest x = *rem;
+                if (beats(x.v, x.i, best.v, best.i)) best = x;
+            }
+            sam[tid] = (best.i == NO_INDEX) ? -1 : best.i;
+        }
+        __syncthreads();
+        uint64_t next = 0;
+        for (int c = 1; c < N; ++c) {
+            const int pc = spar[c];
+            if (((frontier >> pc) & 1ull) && sam[pc] >= 0 && stok[c] == sam[pc]) next |= 1ull << c;
+        }
+        if (next == 0) {
+            chosen = __ffsll((long long)frontier) - 1;
+            break;
+        }
+        frontier = next;
+        par ^= 1;
+    }
+    cluster.sync();  // no CTA leaves while others may still read its exchange slots
+    if (rank == 0) {
+        if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+        else write_path(p, b, spar, stok, chosen, sam[chosen]);
+    }
+}
+
+__global__ void __launch_bounds__(ACC_THREADS)
+accept_stochastic_kernel(AccParams p) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / C;
+    __shared__ int spar[64], stok[64];
+    __shared__ uint64_t wsum[ACC_WARPS];
+    __shared__ uint64_t xsum[2];   // this CTA's slice sum, per attempt
+    __shared__ int xidx;           // token found by this CTA (-1: none)
+    __shared__ int sflag;
+    const int tid = threadIdx.x, N = p.N;
+    if (tid == 0) {
+        sflag = 0;
+        xidx = -1;
+    }
+    __syncthreads();
+    if (tid < N) {
+        spar[tid] = p.parents[(int64_t)b * N + tid];
+        stok[tid] = p.tokens[(int64_t)b * N + tid];
+    }
+    __syncthreads();
+    if (tid == 0) sflag = check_inputs(spar, stok, N, p.V, true);
+    __syncthreads();
+    if (sflag != TV_OK) {
+        if (rank == 0) write_fail(p, b, sflag);
+        return;
+    }
+    // accept tests (every CTA, redundantly: a few scalars)
+    const int K = N - 1;
+    int kstar = K + 1;  // first rejected position, K+1 = none
+    for (int k = 1; k <= K; ++k) {
+        const uint4 w = draw(p, b, k);
+        const uint32_t u24 = w.x >> 8;
+        const int x = stok[k];
+        const float pk = __ldg(p.target + ((int64_t)b * N + (k - 1)) * p.V + x);
+        const float qk = __ldg(p.draft + ((int64_t)b * N + k) * p.V + x);
+        const bool acc = __dmul_rn((double)u24, (double)qk) < __dmul_rn((double)pk, 16777216.0);
+        if (!acc) {
+            kstar = k;
+            break;
+        }
+    }
+    const bool rejected = kstar <= K;
+    const float* rowa = p.target + ((int64_t)b * N + (rejected ? kstar - 1 : K)) * p.V;
+    const float* rowb = rejected ? p.draft + ((int64_t)b * N + kstar) * p.V : nullptr;
+    const uint32_t x1 = draw(p, b, rejected ? kstar : K + 1).y;
+    const Slice sl = make_slice(p.V, C, rank);
+
+    bool resid = rejected;
+    int token = -1;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const uint64_t mine = slice_weight_sum(rowa, rowb, resid, sl, wsum);
+        if (tid == 0) xsum[attempt] = mine;
+        cluster.sync();
+        uint64_t S = 0, before = 0;
+        for (int r = 0; r < C; ++r) {
+            const uint64_t v = *cluster.map_shared_rank(&xsum[attempt], r);
+            if (r < rank) before += v;
+            S += v;
+        }
+        if (S == 0) {
+            if (resid) {
+                resid = false;  // residual has no mass: draw from the target row itself
+                continue;
+            }
+            break;  // zero-mass target row
+        }
+        const uint64_t hi = __umul64hi((uint64_t)x1, S), lo = (uint64_t)x1 * S;
+        const uint64_t T = (hi << 32) | (lo >> 32);
+        if (T >= before && T < before + mine && tid < 32) {
+            const int t = slice_find(rowa, rowb, resid, sl, wsum, T - before);
+            if (tid == 0) xidx = t;
+        }
+        cluster.sync();
+        if (rank == 0) {
+            for (int r = 0; r < C; ++r) {
+                const int v = *cluster.map_shared_rank(&xidx, r);
+                if (v >= 0) token = v;
+            }
+        }
+        break;
+    }
+    cluster.sync();  // exchange slots stay alive until every CTA has read them
+    if (rank == 0) {
+        __shared__ int stoken;
+        if (tid == 0) stoken = token;
+        __syncthreads();
+        if (stoken < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+        else write_path(p, b, spar, stok, rejected ? kstar - 1 : K, stoken);
+    }
+}
+
+int pick_cluster(int B) {
+    // large clusters for small batches (more SMs per row), portable 8 otherwise
+    static int max16 = -1;
+    if (max16 < 0) {
+        max16 = 0;
+        if (cudaFuncSetAttribute(accept_greedy_kernel<true>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaFuncSetAttribute(accept_greedy_kernel<false>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+            cudaFuncSetAttribute(accept_stochastic_kernel,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(16);
+            cfg.blockDim = dim3(ACC_THREADS);
+            cudaLaunchAttribute at;
+            at.id = cudaLaunchAttributeClusterDimension;
+            at.val.clusterDim.x = 16;
+            at.val.clusterDim.y = 1;
+            at.val.clusterDim.z = 1;
+            cfg.attrs = &at;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, accept_greedy_kernel<true>, &cfg) == cudaSuccess &&
+                n > 0)
+                max16 = 1;
+        }
+        cudaGetLastError();
+    }
+    const int sms = device_sm_count();
+    if (max16 && (int64_t)B * 16 <= 2LL * sms) return 16;
+    return 8;
+}
+
+}  // namespace
+
+tv_status launch_accept(const AcceptArgs& a) {
+    if (a.B == 0) return TV_OK;
+    AccParams p;
+    p.parents = a.parents;
+    p.tokens = a.tokens;
+    p.target = a.target;
+    p.draft = a.draft;
+    p.B = a.B;
+    p.N = a.N;
+    p.V = a.V;
+    p.seed = a.seed;
+    p.offset = a.offset;
+    p.accept_len = a.accept_len;
+    p.path = a.path;
+    p.out_tokens = a.out_tokens;
+    p.max_path = a.max_path;
+    p.status = a.status;
+    int C = pick_cluster(a.B);
+    while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.B * C);
+    cfg.blockDim = dim3(ACC_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = C;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (a.mode == TV_ACCEPT_GREEDY) {
+        const bool vec = (a.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0);
+        e = vec ? cudaLaunchKernelEx(&cfg, accept_greedy_kernel<true>, p)
+                : cudaLaunchKernelEx(&cfg, accept_greedy_kernel<false>, p);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, p);
+    }
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // namespace tv

@@ -1,0 +1,51 @@
+// tree_mask_build: parent array -> ancestor-or-self bitmask and depth.
+// One warp per sequence; lanes own nodes lane and lane + 32.  The parent
+// array is staged in shared memory and each node walks its root path there
+// (at most 63 steps: parents strictly decrease along the walk).
+#include "tv_device.cuh"
+#include "tv_internal.h"
+
+namespace tv {
+
+constexpr int kMaskWarps = 4;
+
+__global__ void __launch_bounds__(32 * kMaskWarps)
+tree_mask_kernel(const int32_t* __restrict__ parents, int B, int N, uint64_t* __restrict__ mask,
+                 int32_t* __restrict__ depth, int32_t* __restrict__ status) {
+    __shared__ int32_t spar[kMaskWarps][64];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kMaskWarps + w;
+    if (b >= B) return;
+    const int32_t* par = parents + (int64_t)b * N;
+    bool ok = true;
+    for (int i = lane; i < 64; i += 32) {
+        int p = (i < N) ? par[i] : 0;
+        spar[w][i] = p;
+        if (i < N) ok = ok && ((i == 0) ? (p == -1) : (p >= 0 && p < i));
+    }
+    __syncwarp();
+    ok = __all_sync(0xffffffffu, ok);
+    for (int i = lane; i < N; i += 32) {
+        uint64_t m = 0;
+        int dep = -1;
+        if (ok) {
+            for (int j = i; j >= 0; j = spar[w][j]) {
+                m |= 1ull << j;
+                ++dep;
+            }
+        }
+        mask[(int64_t)b * N + i] = m;
+        if (depth) depth[(int64_t)b * N + i] = ok ? dep : -1;
+    }
+    if (lane == 0) status[b] = ok ? TV_OK : TV_ERR_BAD_TREE;
+}
+
+tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask, int32_t* depth,
+                           int32_t* status, cudaStream_t stream) {
+    if (B == 0) return TV_OK;
+    dim3 grid((B + kMaskWarps - 1) / kMaskWarps);
+    tree_mask_kernel<<<grid, 32 * kMaskWarps, 0, stream>>>(parents, B, N, mask, depth, status);
+    return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+}
+
+}  // namespace tv

@@ -1,0 +1,75 @@
+// Host-side interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "treeverify.h"
+
+namespace tv {
+
+// Multiprocessor count and opt-in shared memory of the current device (cached per device).
+int device_sm_count();
+int device_smem_optin();
+
+struct AttnArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* prefix_lens;
+    const uint64_t* mask;
+    int B, N, Hq, Hkv, d, bs, num_blocks;
+    float scale;
+    void* out;
+    int32_t* status;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask, int32_t* depth,
+                           int32_t* status, cudaStream_t stream);
+tv_status launch_attn_f32(const AttnArgs& a);
+size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs);
+tv_status launch_attn_bf16(const AttnArgs& a);
+
+struct AcceptArgs {
+    tv_accept_mode mode;
+    const int32_t* parents;
+    const int32_t* tokens;
+    const float* target;
+    const float* draft;
+    int B, N, V;
+    uint64_t seed, offset;
+    int32_t* accept_len;
+    int32_t* path;
+    int32_t* out_tokens;
+    int max_path;
+    int32_t* status;
+    cudaStream_t stream;
+};
+tv_status launch_accept(const AcceptArgs& a);
+
+struct CompactArgs {
+    void* k_cache;
+    void* v_cache;
+    int num_layers;
+    int64_t layer_stride;
+    const int32_t* block_table;
+    int max_blocks;
+    const int32_t* prefix_lens;
+    const int32_t* path;
+    const int32_t* accept_len;
+    int max_path, B, Hkv, d, bs, num_blocks, elem_bytes;
+    int32_t* new_lens;
+    int64_t* src_slots;
+    int64_t* dst_slots;
+    int32_t* status;
+    cudaStream_t stream;
+};
+tv_status launch_compact(const CompactArgs& a);
+
+}  // namespace tv

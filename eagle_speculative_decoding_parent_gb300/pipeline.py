@@ -1,0 +1,63 @@
+"""One verification step through the four entry points, with its buffers.
+
+A convenience for callers that hold torch tensors: it owns the outputs and
+the attention workspace and issues, in stream order,
+tree_mask_build -> tree_verify_attention -> tree_accept -> kv_compact.
+Marshalling only; the arithmetic is in the CUDA library.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (GREEDY, STOCHASTIC, kv_compact, tree_accept, tree_mask_build,
+               tree_verify_attention, tree_verify_attention_workspace)
+
+
+class VerifyStep:
+    def __init__(self, *, B, N, Hq, Hkv, d, max_blocks, bs, dtype, max_path, device="cuda"):
+        self.B, self.N, self.Hq, self.Hkv, self.d = B, N, Hq, Hkv, d
+        self.max_path = max_path
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.mask = torch.zeros((B, N), dtype=torch.int64, device=dev)
+        self.depth = torch.zeros((B, N), **i32)
+        self.st_mask = torch.zeros(B, **i32)
+        self.out = torch.zeros((B, N, Hq, d), dtype=dtype, device=dev)
+        self.st_attn = torch.zeros(B, **i32)
+        self.accept_len = torch.zeros(B, **i32)
+        self.path = torch.zeros((B, max_path), **i32)
+        self.out_tokens = torch.zeros((B, max_path), **i32)
+        self.st_accept = torch.zeros(B, **i32)
+        self.new_lens = torch.zeros(B, **i32)
+        self.src_slots = torch.zeros((B, max_path), dtype=torch.int64, device=dev)
+        self.dst_slots = torch.zeros((B, max_path), dtype=torch.int64, device=dev)
+        self.st_compact = torch.zeros(B, **i32)
+        ws = tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_blocks, bs, dtype)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+
+    def mask_build(self, parents, stream=None):
+        tree_mask_build(parents, self.mask, self.depth, self.st_mask, stream=stream)
+
+    def attention(self, q, k_cache, v_cache, block_table, prefix_lens, stream=None):
+        tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, self.mask, self.out,
+                              self.st_attn, self.workspace, stream=stream)
+
+    def accept(self, mode, parents, draft_tokens, target, draft_probs=None, seed=0, offset=0,
+               stream=None):
+        tree_accept(mode, parents, draft_tokens, target, draft_probs, self.accept_len, self.path,
+                    self.out_tokens, self.st_accept, seed=seed, offset=offset, stream=stream)
+
+    def compact(self, k_cache, v_cache, block_table, prefix_lens, stream=None):
+        kv_compact(k_cache, v_cache, block_table, prefix_lens, self.path, self.accept_len,
+                   self.new_lens, self.st_compact, src_slots=self.src_slots,
+                   dst_slots=self.dst_slots, stream=stream)
+
+    def run(self, *, parents, q, k_cache, v_cache, block_table, prefix_lens, draft_tokens, target,
+            draft_probs=None, mode=GREEDY, seed=0, offset=0, stream=None):
+        self.mask_build(parents, stream)
+        self.attention(q, k_cache, v_cache, block_table, prefix_lens, stream)
+        self.accept(mode, parents, draft_tokens, target, draft_probs, seed, offset, stream)
+        self.compact(k_cache, v_cache, block_table, prefix_lens, stream)
+
+
+__all__ = ["VerifyStep", "GREEDY", "STOCHASTIC"]

@@ -1,0 +1,80 @@
+"""The C-ABI library (CPU only, no GPU needed): it builds, loads, exports
+every function include/treeverify.h declares, and rejects bad arguments on
+the host before touching the GPU."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "treeverify.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                                 text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    bm = __graft_entry__._build_module()
+    if not os.path.exists(bm.LIB) and not shutil.which("nvcc"):
+        pytest.skip("library not built and nvcc unavailable")
+    return ctypes.CDLL(bm.build())
+
+
+def test_header_declares_the_four_steps():
+    fns = declared_functions()
+    for name in ("tree_mask_build", "tree_verify_attention", "tree_accept", "kv_compact",
+                 "tree_verify_attention_workspace", "tree_accept_workspace",
+                 "tv_status_string", "tv_abi_version"):
+        assert name in fns, fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    lib.tv_status_string.restype = ctypes.c_char_p
+    for code in range(9):
+        assert lib.tv_status_string(code)
+    assert lib.tv_status_string(99) == b"unknown status"
+    assert lib.tv_abi_version() == 1
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    p = ctypes.c_void_p
+    # N outside [1, 64]
+    assert lib.tree_mask_build(p(0), 1, 65, p(0), p(0), p(0), p(0)) == 1
+    assert lib.tree_mask_build(p(0), -1, 4, p(0), p(0), p(0), p(0)) == 1
+    # B == 0: nothing to do, no launch
+    assert lib.tree_mask_build(p(0), 0, 4, p(0), p(0), p(0), p(0)) == 0
+    # stochastic acceptance needs draft probabilities
+    f = lib.tree_accept
+    f.argtypes = [ctypes.c_int, p, p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_uint64, ctypes.c_uint64, p, p, p, ctypes.c_int, p, p, ctypes.c_size_t, p]
+    nz = p(16)
+    assert f(1, nz, nz, nz, None, 2, 4, 10, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1
+    assert f(0, nz, nz, nz, None, 2, 4, 0, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1  # V = 0
+    # attention: head size 96 is not built for bf16 -> unsupported
+    a = lib.tree_verify_attention
+    a.argtypes = [p, p, p, p, ctypes.c_int, p, p] + [ctypes.c_int] * 8 + \
+        [ctypes.c_float, p, p, p, ctypes.c_size_t, p]
+    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, 8, 2, 96, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
+             None) == 4
+    # Hq not a multiple of Hkv -> invalid
+    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, 6, 4, 128, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
+             None) == 1
+    # kv_compact: rows that are not a multiple of 16 bytes -> unsupported
+    c = lib.kv_compact
+    c.argtypes = [p, p, ctypes.c_int, ctypes.c_int64, p, ctypes.c_int, p, p, p] + \
+        [ctypes.c_int] * 7 + [p, p, p, p, p]
+    assert c(nz, nz, 1, 0, nz, 4, nz, nz, nz, 4, 2, 2, 12, 16, 10, 1, nz, None, None, nz,
+             None) == 4

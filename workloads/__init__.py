@@ -87,10 +87,14 @@ DEFAULT_BENCH = "llama3_8b_tree60"
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
-    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    """Round finite float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
+    flat = np.ascontiguousarray(x, np.float32).reshape(-1).view(np.uint32)
+    out = np.empty(flat.shape, np.uint16)
+    step = 1 << 24
+    for s in range(0, flat.size, step):       # bounded temporaries for large caches
+        u = flat[s:s + step]
+        out[s:s + step] = ((u + (0x7FFF + ((u >> 16) & 1))) >> 16).astype(np.uint16)
+    return out.reshape(np.shape(x))
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
