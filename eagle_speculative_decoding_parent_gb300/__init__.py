@@ -23,7 +23,8 @@ from . import _build
 __all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTED",
            "TV_ERR_TIMEOUT", "TV_ERR_BAD_VALUES", "TV_F32", "TV_BF16", "GREEDY", "STOCHASTIC",
            "TreeVerifyError", "library_path", "status_string", "tree_mask_build",
-           "tree_verify_attention_workspace", "tree_verify_attention", "tree_accept_workspace",
+           "tree_verify_attention_workspace", "tree_verify_attention",
+           "tree_accept_workspace",
            "tree_accept", "kv_compact"]
 
 (TV_OK, TV_ERR_INVALID_ARG, TV_ERR_BAD_TREE, TV_ERR_OUT_OF_RANGE, TV_ERR_UNSUPPORTED,

@@ -156,7 +156,27 @@ __device__ uint64_t slice_weight_sum(const float* a, const float* bq, bool resid
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int slo = min(s.hi, s.lo + warp * s.seg), shi = min(s.hi, slo + s.seg);
     uint64_t acc = 0;
-    for (int t = slo + lane; t < shi; t += 32) acc += elem_weight(a, bq, t, resid);
+    const bool vec = ((reinterpret_cast<uintptr_t>(a + slo) | (bq ? reinterpret_cast<uintptr_t>(bq + slo) : 0)) & 15) == 0;
+    int t = slo;
+    if (vec) {
+        // four floats per lane per step, four steps in flight
+        const int nv4 = (shi - slo) >> 2;
+        const float4* a4 = reinterpret_cast<const float4*>(a + slo);
+        const float4* b4 = resid ? reinterpret_cast<const float4*>(bq + slo) : nullptr;
+#pragma unroll 4
+        for (int e = lane; e < nv4; e += 32) {
+            const float4 x = __ldg(a4 + e);
+            if (resid) {
+                const float4 y = __ldg(b4 + e);
+                acc += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
+                       weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
+            } else {
+                acc += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
+            }
+        }
+        t = slo + 4 * nv4;
+    }
+    for (t += lane; t < shi; t += 32) acc += elem_weight(a, bq, t, resid);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     __syncthreads();
@@ -294,34 +314,138 @@ accept_greedy_kernel(AccParams p) {
             if (tid == 0) exch[par][u] = a;
         }
         cluster.sync();
-        // combine across the cluster (thread u handles frontier node u)
-        if (tid < N && ((frontier >> tid) & 1ull)) {
-            ArgBest best{-INFINITY, NO_INDEX};
-            for (int r = 0; r < C; ++r) {
-                const ArgBest* rem = cluster.map_shared_rank(&exch[par][tid], r);
-                const ArgBest x = *rem;
-                if (beats(x.v, x.i, best.v, best.i)) best = x;
+        // combine across the cluster: warp w takes frontier nodes w, w+16, ...;
+        // lane r reads rank r's candidate, then a warp argmax
+        {
+            const int warp = tid >> 5, lane = tid & 31;
+            int idx = 0;
+            for (uint64_t f = frontier; f; f &= f - 1, ++idx) {
+                if (idx % ACC_WARPS != warp) continue;
+                const int u = __ffsll((long long)f) - 1;
+                ArgBest x{-INFINITY, NO_INDEX};
+                if (lane < C) x = *cluster.map_shared_rank(&exch[par][u], lane);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
+                    const int j = __shfl_xor_sync(0xffffffffu, x.i, off);
+                    if (beats(w, j, x.v, x.i)) {
+                        x.v = w;
+                        x.i = j;
+                    }
+                }
+                if (lane == 0) sam[u] = (x.i == NO_INDEX) ? -1 : x.i;
             }
-            sam[tid] = (best.i == NO_INDEX) ? -1 : best.i;
         }
         __syncthreads();
-        uint64_t next = 0;
-        for (int c = 1; c < N; ++c) {
-            const int pc = spar[c];
-            if (((frontier >> pc) & 1ull) && sam[pc] >= 0 && stok[c] == sam[pc]) next |= 1ull << c;
+        // next frontier: children whose token equals their (frontier) parent's argmax
+        __shared__ unsigned long long snext;
+        if (tid == 0) snext = 0ull;
+        __syncthreads();
+        if (tid >= 1 && tid < N) {
+            const int pc = spar[tid];
+            if (((frontier >> pc) & 1ull) && sam[pc] >= 0 && stok[tid] == sam[pc])
+                atomicOr(&snext, 1ull << tid);
         }
+        __syncthreads();
+        const uint64_t next = snext;
         if (next == 0) {
             chosen = __ffsll((long long)frontier) - 1;
             break;
         }
         frontier = next;
         par ^= 1;
+        __syncthreads();  // snext is reset at the next level
     }
     cluster.sync();  // no CTA leaves while others may still read its exchange slots
     if (rank == 0) {
         if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
         else write_path(p, b, spar, stok, chosen, sam[chosen]);
     }
+}
+
+// Greedy acceptance for small batches: every row's argmax is computed in
+// parallel (one cluster per row, DSMEM reduction), written to the workspace,
+// and the CTA that completes a sequence's last row (atomic ticket) walks the
+// tree.  Reads every row once, but without the walk's level-by-level latency.
+template <bool VEC>
+__global__ void __launch_bounds__(ACC_THREADS)
+accept_rowscan_kernel(AccParams p, int32_t* __restrict__ am_ws, int32_t* __restrict__ tickets) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int cl = blockIdx.x / S;
+    const int N = p.N;
+    const int b = cl / N, row = cl % N;
+    const int tid = threadIdx.x;
+    __shared__ ArgBest red[ACC_WARPS];
+    __shared__ ArgBest exch;
+    __shared__ int last;
+    __shared__ int spar[64], stok[64], sam[64];
+    __shared__ int sflag;
+    const Slice sl = make_slice(p.V, S, rank);
+    const ArgBest a = block_argmax<VEC>(p.target + ((int64_t)b * N + row) * p.V, sl.lo, sl.hi, red);
+    if (tid == 0) exch = a;
+    cluster.sync();
+    if (rank == 0 && tid < 32) {
+        ArgBest x{-INFINITY, NO_INDEX};
+        if (tid < S) x = *cluster.map_shared_rank(&exch, tid);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
+            const int j = __shfl_xor_sync(0xffffffffu, x.i, off);
+            if (beats(w, j, x.v, x.i)) {
+                x.v = w;
+                x.i = j;
+            }
+        }
+        if (tid == 0) {
+            am_ws[(int64_t)b * N + row] = (x.i == NO_INDEX) ? -1 : x.i;
+            __threadfence();
+            last = (atomicAdd(&tickets[b], 1) == N - 1);
+        }
+    }
+    cluster.sync();  // peers' exchange slots stay alive until rank 0 has read them
+    if (rank != 0) return;
+    __syncthreads();
+    if (!last) return;
+    // this CTA completed sequence b: walk its tree
+    __threadfence();
+    if (tid < N) {
+        spar[tid] = p.parents[(int64_t)b * N + tid];
+        stok[tid] = p.tokens[(int64_t)b * N + tid];
+        sam[tid] = __ldcg(am_ws + (int64_t)b * N + tid);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        tickets[b] = 0;  // leave the workspace ready for the next call
+        sflag = check_inputs(spar, stok, N, p.V, false);
+    }
+    __syncthreads();
+    if (sflag != TV_OK) {
+        write_fail(p, b, sflag);
+        return;
+    }
+    __shared__ int schosen;
+    if (tid == 0) {
+        // accepted(c) = accepted(parent) and token(c) == argmax(parent row); topological order
+        uint64_t acc = 1ull;
+        int dep[64];
+        dep[0] = 0;
+        int chosen = 0;
+        for (int c = 1; c < N; ++c) {
+            const int pc = spar[c];
+            dep[c] = dep[pc] + 1;
+            if (((acc >> pc) & 1ull) && sam[pc] >= 0 && stok[c] == sam[pc]) {
+                acc |= 1ull << c;
+                if (dep[c] > dep[chosen]) chosen = c;
+            }
+        }
+        schosen = chosen;
+    }
+    __syncthreads();
+    const int chosen = schosen;
+    if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+    else write_path(p, b, spar, stok, chosen, sam[chosen]);
 }
 
 __global__ void __launch_bounds__(ACC_THREADS)
@@ -417,17 +541,22 @@ accept_stochastic_kernel(AccParams p) {
     }
 }
 
-int pick_cluster(int B) {
-    // large clusters for small batches (more SMs per row), portable 8 otherwise
-    static int max16 = -1;
-    if (max16 < 0) {
-        max16 = 0;
-        if (cudaFuncSetAttribute(accept_greedy_kernel<true>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-            cudaFuncSetAttribute(accept_greedy_kernel<false>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-            cudaFuncSetAttribute(accept_stochastic_kernel,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+// Allows 16-CTA clusters for every kernel here when the device supports it.
+bool enable_large_clusters() {
+    static int state = -1;
+    if (state < 0) {
+        state = 0;
+        bool ok = cudaFuncSetAttribute(accept_greedy_kernel<true>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        ok = ok && cudaFuncSetAttribute(accept_greedy_kernel<false>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        ok = ok && cudaFuncSetAttribute(accept_rowscan_kernel<true>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        ok = ok && cudaFuncSetAttribute(accept_rowscan_kernel<false>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        ok = ok && cudaFuncSetAttribute(accept_stochastic_kernel,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        if (ok) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(16);
             cfg.blockDim = dim3(ACC_THREADS);
@@ -439,18 +568,38 @@ int pick_cluster(int B) {
             cfg.attrs = &at;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, accept_greedy_kernel<true>, &cfg) == cudaSuccess &&
-                n > 0)
-                max16 = 1;
+            ok = cudaOccupancyMaxActiveClusters(&n, accept_greedy_kernel<true>, &cfg) == cudaSuccess &&
+                 n > 0;
         }
         cudaGetLastError();
+        state = ok ? 1 : 0;
     }
-    const int sms = device_sm_count();
-    if (max16 && (int64_t)B * 16 <= 2LL * sms) return 16;
-    return 8;
+    return state == 1;
 }
 
+int pow2_at_least(int64_t x) {
+    int c = 1;
+    while (c < x && c < 16) c <<= 1;
+    return c;
+}
+
+// Row-scan pays for every row once at full bandwidth; the walk pays a few
+// microseconds of latency per tree level (at most 8 levels assumed).
+bool prefer_rowscan(int B, int N, int V) {
+    const double bytes = (double)B * N * V * 4.0;
+    const double t_scan = bytes / 6.0e12 + 3.0e-6;
+    const double t_walk = (double)(N < 8 ? N : 8) * 2.5e-6;
+    return t_scan < t_walk;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
 }  // namespace
+
+size_t accept_workspace(tv_accept_mode mode, int B, int N, int V) {
+    if (mode != TV_ACCEPT_GREEDY || B <= 0 || !prefer_rowscan(B, N, V)) return 0;
+    return align256((size_t)B * N * 4) + align256((size_t)B * 4);
+}
 
 tv_status launch_accept(const AcceptArgs& a) {
     if (a.B == 0) return TV_OK;
@@ -469,10 +618,28 @@ tv_status launch_accept(const AcceptArgs& a) {
     p.out_tokens = a.out_tokens;
     p.max_path = a.max_path;
     p.status = a.status;
-    int C = pick_cluster(a.B);
+    const bool large = enable_large_clusters();
+    const int cmax = large ? 16 : 8;
+    const int sms = device_sm_count();
+    const bool vec = (a.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0);
+    const size_t need = accept_workspace(a.mode, a.B, a.N, a.V);
+    if (need > 0 && (a.ws == nullptr || a.ws_bytes < need)) return TV_ERR_WORKSPACE;
+    const bool rowscan = need > 0;
+
+    int C;
+    int64_t units;
+    if (rowscan) {
+        units = (int64_t)a.B * a.N;
+        C = pow2_at_least((2LL * sms + units - 1) / units);
+    } else {
+        units = a.B;
+        C = ((int64_t)a.B * 16 <= 2LL * sms) ? 16 : 8;
+    }
+    if (C > cmax) C = cmax;
     while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
+    if (units * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.B * C);
+    cfg.gridDim = dim3((unsigned)(units * C));
     cfg.blockDim = dim3(ACC_THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.stream;
@@ -484,8 +651,13 @@ tv_status launch_accept(const AcceptArgs& a) {
     cfg.attrs = &at;
     cfg.numAttrs = 1;
     cudaError_t e;
-    if (a.mode == TV_ACCEPT_GREEDY) {
-        const bool vec = (a.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0);
+    if (a.mode == TV_ACCEPT_GREEDY && rowscan) {
+        int32_t* am = static_cast<int32_t*>(a.ws);
+        int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.ws) +
+                                                       align256((size_t)a.B * a.N * 4));
+        e = vec ? cudaLaunchKernelEx(&cfg, accept_rowscan_kernel<true>, p, am, tickets)
+                : cudaLaunchKernelEx(&cfg, accept_rowscan_kernel<false>, p, am, tickets);
+    } else if (a.mode == TV_ACCEPT_GREEDY) {
         e = vec ? cudaLaunchKernelEx(&cfg, accept_greedy_kernel<true>, p)
                 : cudaLaunchKernelEx(&cfg, accept_greedy_kernel<false>, p);
     } else {

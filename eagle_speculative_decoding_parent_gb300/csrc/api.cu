@@ -119,11 +119,8 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
 }
 
 size_t tree_accept_workspace(tv_accept_mode mode, int B, int N, int V) {
-    (void)mode;
-    (void)B;
-    (void)N;
-    (void)V;
-    return 0;
+    if (B <= 0 || N < 1 || N > 64 || V < 1 || V > (1 << 24)) return 0;
+    return accept_workspace(mode, B, N, V);
 }
 
 tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t* draft_tokens,
@@ -131,8 +128,6 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
                       uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* path,
                       int32_t* out_tokens, int max_path, int32_t* status, void* workspace,
                       size_t workspace_bytes, tv_stream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (mode != TV_ACCEPT_GREEDY && mode != TV_ACCEPT_STOCHASTIC) return TV_ERR_INVALID_ARG;
     if (B < 0 || N < 1 || N > 64 || V < 1 || V > (1 << 24) || max_path < 1)
         return TV_ERR_INVALID_ARG;
@@ -157,6 +152,8 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
     a.out_tokens = out_tokens;
     a.max_path = max_path;
     a.status = status;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
     a.stream = (cudaStream_t)stream;
     return launch_accept(a);
 }

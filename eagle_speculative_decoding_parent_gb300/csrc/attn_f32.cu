@@ -82,14 +82,25 @@ attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
         l_run = l_run * corr + psum;
 #pragma unroll
         for (int k = 0; k < DPL; ++k) acc[k] *= corr;
-        uint32_t vmask = __ballot_sync(0xffffffffu, vis);
-        while (vmask) {
-            const int j = __ffs(vmask) - 1;
-            vmask &= vmask - 1;
-            const float pj = __shfl_sync(0xffffffffu, p, j);
-            const float* vr = vc + row_of(t0 + j);
+        // value rows of the visible keys, eight keys per batch of independent loads
+        const uint32_t vmask = __ballot_sync(0xffffffffu, vis);
+        const int64_t my_row = vis ? row_of(t) : 0;
+#pragma unroll 1
+        for (int j0 = 0; j0 < 32; j0 += 8) {
+            float vv[8][DPL];
 #pragma unroll
-            for (int k = 0; k < DPL; ++k) acc[k] = fmaf(pj, vr[lane + 32 * k], acc[k]);
+            for (int jj = 0; jj < 8; ++jj) {
+                const int64_t rj = __shfl_sync(0xffffffffu, my_row, j0 + jj);
+                const bool use = (vmask >> (j0 + jj)) & 1u;
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) vv[jj][k] = use ? __ldg(vc + rj + lane + 32 * k) : 0.f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const float pj = __shfl_sync(0xffffffffu, p, j0 + jj);
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) acc[k] = fmaf(pj, vv[jj][k], acc[k]);
+            }
         }
         m_run = m_new;
     }

@@ -34,6 +34,9 @@ tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask,
                            int32_t* status, cudaStream_t stream);
 tv_status launch_attn_f32(const AttnArgs& a);
 size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs);
+// Leading bytes of that workspace that must be zero when a call starts.
+size_t attn_bf16_workspace_zeroed_prefix(int B, int N, int Hq, int Hkv, int d, int max_blocks,
+                                         int bs);
 tv_status launch_attn_bf16(const AttnArgs& a);
 
 struct AcceptArgs {
@@ -49,8 +52,11 @@ struct AcceptArgs {
     int32_t* out_tokens;
     int max_path;
     int32_t* status;
+    void* ws;
+    size_t ws_bytes;
     cudaStream_t stream;
 };
+size_t accept_workspace(tv_accept_mode mode, int B, int N, int V);
 tv_status launch_accept(const AcceptArgs& a);
 
 struct CompactArgs {

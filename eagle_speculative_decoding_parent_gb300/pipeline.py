@@ -9,12 +9,13 @@ from __future__ import annotations
 
 import torch
 
-from . import (GREEDY, STOCHASTIC, kv_compact, tree_accept, tree_mask_build,
-               tree_verify_attention, tree_verify_attention_workspace)
+from . import (GREEDY, STOCHASTIC, kv_compact, tree_accept, tree_accept_workspace,
+               tree_mask_build, tree_verify_attention, tree_verify_attention_workspace)
 
 
 class VerifyStep:
-    def __init__(self, *, B, N, Hq, Hkv, d, max_blocks, bs, dtype, max_path, device="cuda"):
+    def __init__(self, *, B, N, Hq, Hkv, d, max_blocks, bs, dtype, max_path, V=1,
+                 mode=GREEDY, device="cuda"):
         self.B, self.N, self.Hq, self.Hkv, self.d = B, N, Hq, Hkv, d
         self.max_path = max_path
         dev = torch.device(device)
@@ -34,6 +35,8 @@ class VerifyStep:
         self.st_compact = torch.zeros(B, **i32)
         ws = tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_blocks, bs, dtype)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
+        aws = tree_accept_workspace(mode, B, N, V)
+        self.accept_workspace = torch.zeros(max(aws, 256), dtype=torch.uint8, device=dev)
 
     def mask_build(self, parents, stream=None):
         tree_mask_build(parents, self.mask, self.depth, self.st_mask, stream=stream)
@@ -45,7 +48,8 @@ class VerifyStep:
     def accept(self, mode, parents, draft_tokens, target, draft_probs=None, seed=0, offset=0,
                stream=None):
         tree_accept(mode, parents, draft_tokens, target, draft_probs, self.accept_len, self.path,
-                    self.out_tokens, self.st_accept, seed=seed, offset=offset, stream=stream)
+                    self.out_tokens, self.st_accept, seed=seed, offset=offset,
+                    workspace=self.accept_workspace, stream=stream)
 
     def compact(self, k_cache, v_cache, block_table, prefix_lens, stream=None):
         kv_compact(k_cache, v_cache, block_table, prefix_lens, self.path, self.accept_len,

@@ -169,8 +169,13 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
  * a path longer than max_path, TV_ERR_UNSUPPORTED for a non-chain in
  * stochastic mode, TV_ERR_BAD_VALUES) the sequence gets accept_len 0, path
  * [0, -1, ...] and out_tokens all -1.
- * workspace: tree_accept_workspace() bytes (currently 0: may be NULL).
- * Host errors: N outside [1, 64], V outside [1, 2^24], max_path < 1.
+ * workspace: at least tree_accept_workspace() bytes (0 means none is needed
+ * and NULL is allowed).  Greedy acceptance on small batches reads every row
+ * once in parallel and keeps one argmax per row plus a per-sequence arrival
+ * counter there; the counters must be zero before the first call (zero the
+ * whole buffer once) and every completed call leaves them at zero.
+ * Host errors: N outside [1, 64], V outside [1, 2^24], max_path < 1;
+ * TV_ERR_WORKSPACE when the workspace is missing or too small.
  * ------------------------------------------------------------------------ */
 size_t tree_accept_workspace(tv_accept_mode mode, int B, int N, int V);
 

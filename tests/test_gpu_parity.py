@@ -240,8 +240,11 @@ def run_accept(tv, w, mode, max_path, seed=0, offset=0):
     path = torch.full((B, max_path), -9, dtype=torch.int32, device="cuda")
     out = torch.full((B, max_path), -9, dtype=torch.int32, device="cuda")
     st = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    V = target.shape[2]
+    aws = tv.tree_accept_workspace(mode, B, N, V)
+    ws = torch.zeros(max(aws, 256), dtype=torch.uint8, device="cuda")
     tv.tree_accept(mode, dev(w["parents"]), dev(w["draft_tokens"]), target, draft, acc, path,
-                   out, st, seed=seed, offset=offset)
+                   out, st, seed=seed, offset=offset, workspace=ws)
     torch.cuda.synchronize()
     return acc.cpu().numpy(), path.cpu().numpy(), out.cpu().numpy(), st.cpu().numpy()
 
@@ -391,9 +394,10 @@ def test_full_step_matches_oracle(tv, orc, name):
     mp = W.max_path_len(w["parents"])
     d = to_device(w)
     dtype = d["q"].dtype
-    step = VerifyStep(B=B, N=N, Hq=spec.Hq, Hkv=spec.Hkv, d=spec.d,
-                      max_blocks=w["block_table"].shape[1], bs=spec.bs, dtype=dtype, max_path=mp)
     mode = 0 if spec.mode == "greedy" else 1
+    step = VerifyStep(B=B, N=N, Hq=spec.Hq, Hkv=spec.Hkv, d=spec.d,
+                      max_blocks=w["block_table"].shape[1], bs=spec.bs, dtype=dtype, max_path=mp,
+                      V=spec.V, mode=mode)
     step.run(parents=d["parents"], q=d["q"], k_cache=d["k_cache"], v_cache=d["v_cache"],
              block_table=d["block_table"], prefix_lens=d["prefix_lens"],
              draft_tokens=d["draft_tokens"], target=d["logits"] if mode == 0 else d["p"],
