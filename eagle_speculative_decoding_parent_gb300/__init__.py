@@ -24,6 +24,7 @@ __all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTE
            "TV_ERR_TIMEOUT", "TV_ERR_BAD_VALUES", "TV_F32", "TV_BF16", "GREEDY", "STOCHASTIC",
            "TreeVerifyError", "library_path", "status_string", "tree_mask_build",
            "tree_verify_attention_workspace", "tree_verify_attention",
+           "tree_verify_attention_noalloc", "tree_verify_attention_noalloc_capacity",
            "tree_accept_workspace",
            "tree_accept", "kv_compact"]
 
@@ -64,6 +65,9 @@ _mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p])
 _attn_ws = _sig("tree_verify_attention_workspace", _sz, [_i, _i, _i, _i, _i, _i, _i, _i])
 _attn = _sig("tree_verify_attention", _i,
              [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p])
+_attn_na = _sig("tree_verify_attention_noalloc", _i,
+                [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p])
+_attn_na_cap = _sig("tree_verify_attention_noalloc_capacity", _sz, [])
 _acc_ws = _sig("tree_accept_workspace", _sz, [_i, _i, _i, _i])
 _acc = _sig("tree_accept", _i,
             [_i, _p, _p, _p, _p, _i, _i, _i, _u64, _u64, _p, _p, _p, _i, _p, _p, _sz, _p])
@@ -146,6 +150,24 @@ def tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, mask, o
                  _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs, num_blocks, dt, scale,
                  _ptr(out), _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)),
            "tree_verify_attention")
+
+
+def tree_verify_attention_noalloc_capacity() -> int:
+    return int(_attn_na_cap())
+
+
+def tree_verify_attention_noalloc(q, k_cache, v_cache, block_table, prefix_lens, mask, out,
+                                  status, *, scale: float = 0.0, stream=None) -> None:
+    """tree_verify_attention without a caller workspace: scratch comes from a
+    fixed array inside the library (see the C header for the constraints)."""
+    B, N, Hq, d = q.shape
+    num_blocks, Hkv, bs, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    _check(_attn_na(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                    block_table.shape[1], _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs,
+                    num_blocks, _dt(q), scale, _ptr(out), _ptr(status), _stream(stream)),
+           "tree_verify_attention_noalloc")
 
 
 def tree_accept_workspace(mode, B, N, V) -> int:

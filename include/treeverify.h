@@ -212,6 +212,42 @@ tv_status kv_compact(void* k_cache, void* v_cache, int num_layers, int64_t layer
                      tv_dtype dt, int32_t* new_lens, int64_t* src_slots, int64_t* dst_slots,
                      int32_t* status, tv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * tree_verify_attention_noalloc — no counterpart on the pages describing the
+ * method; an addition of this library for callers that cannot allocate.
+ *
+ * Some callers cannot provide device scratch memory: an engine that reserved
+ * all of HBM for its own pools up front and does not allocate while decoding,
+ * or a plugin host that gives its plugins no allocator.  This call computes
+ * exactly what tree_verify_attention computes (same arguments, minus the
+ * workspace) but takes its scratch from a fixed array inside the library:
+ * TV_NOALLOC_SCRATCH_BYTES of device memory that every GPU loading the
+ * library holds until the process exits.  It never calls cudaMalloc,
+ * cudaFree or any allocating routine.
+ *
+ * - Sizes whose workspace (tree_verify_attention_workspace) exceeds
+ *   TV_NOALLOC_SCRATCH_BYTES are rejected with TV_ERR_WORKSPACE before
+ *   anything is launched.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture begins.
+ * - All calls share the one array, and it keeps the previous call's
+ *   contents: each call first clears (cudaMemsetAsync on `stream`) the part
+ *   that must start at zero.  Calls that overlap on the GPU (different
+ *   streams, or concurrent host threads) race on the array and must not be
+ *   issued.
+ * ------------------------------------------------------------------------ */
+#define TV_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+
+size_t tree_verify_attention_noalloc_capacity(void);
+
+tv_status tree_verify_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* prefix_lens, const uint64_t* mask, int B,
+                                        int N, int Hq, int Hkv, int d, int block_size,
+                                        int num_blocks, tv_dtype dt, float scale, void* out,
+                                        int32_t* status, tv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
