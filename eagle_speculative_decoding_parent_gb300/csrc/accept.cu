@@ -57,10 +57,16 @@ __device__ __forceinline__ bool beats(float v, int i, float w, int j) {
 }
 
 __device__ __forceinline__ void take(ArgBest& a, float x, int i) {
-    if (!isnan(x) && beats(x, i, a.v, a.i)) {
-        a.v = x;
-        a.i = i;
-    }
+    const bool better = !isnan(x) && beats(x, i, a.v, a.i);
+    a.v = better ? x : a.v;
+    a.i = better ? i : a.i;
+}
+
+__device__ __forceinline__ void take4(ArgBest& a, const float4& x, int i) {
+    take(a, x.x, i);
+    take(a, x.y, i + 1);
+    take(a, x.z, i + 2);
+    take(a, x.w, i + 3);
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), written from the published
@@ -118,15 +124,18 @@ __device__ ArgBest block_argmax(const float* __restrict__ row, int lo, int hi, A
     if (VEC) {
         const int nv = (hi - lo) >> 2;
         const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-#pragma unroll 4
-        for (int e = tid; e < nv; e += ACC_THREADS) {
-            const float4 x = __ldg(r4 + e);
-            const int i = lo + 4 * e;
-            take(a, x.x, i);
-            take(a, x.y, i + 1);
-            take(a, x.z, i + 2);
-            take(a, x.w, i + 3);
+        constexpr int T = ACC_THREADS;
+        int e = tid;
+        // four independent 16-byte loads in flight before any compare
+        for (; e + 3 * T < nv; e += 4 * T) {
+            const float4 x0 = __ldg(r4 + e), x1 = __ldg(r4 + e + T);
+            const float4 x2 = __ldg(r4 + e + 2 * T), x3 = __ldg(r4 + e + 3 * T);
+            take4(a, x0, lo + 4 * e);
+            take4(a, x1, lo + 4 * (e + T));
+            take4(a, x2, lo + 4 * (e + 2 * T));
+            take4(a, x3, lo + 4 * (e + 3 * T));
         }
+        for (; e < nv; e += T) take4(a, __ldg(r4 + e), lo + 4 * e);
         for (int i = lo + 4 * nv + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
     } else {
         for (int i = lo + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
@@ -163,17 +172,23 @@ __device__ uint64_t slice_weight_sum(const float* a, const float* bq, bool resid
         const int nv4 = (shi - slo) >> 2;
         const float4* a4 = reinterpret_cast<const float4*>(a + slo);
         const float4* b4 = resid ? reinterpret_cast<const float4*>(bq + slo) : nullptr;
-#pragma unroll 4
-        for (int e = lane; e < nv4; e += 32) {
-            const float4 x = __ldg(a4 + e);
-            if (resid) {
-                const float4 y = __ldg(b4 + e);
-                acc += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
+        auto wsum4 = [&](const float4& x, const float4& y) -> uint64_t {
+            if (resid)
+                return weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
                        weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
-            } else {
-                acc += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
-            }
+            return weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
+        };
+        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        int e = lane;
+        // four independent loads per operand in flight before any use
+        for (; e + 96 < nv4; e += 128) {
+            const float4 x0 = __ldg(a4 + e), x1 = __ldg(a4 + e + 32);
+            const float4 x2 = __ldg(a4 + e + 64), x3 = __ldg(a4 + e + 96);
+            const float4 y0 = resid ? __ldg(b4 + e) : zero4, y1 = resid ? __ldg(b4 + e + 32) : zero4;
+            const float4 y2 = resid ? __ldg(b4 + e + 64) : zero4, y3 = resid ? __ldg(b4 + e + 96) : zero4;
+            acc += wsum4(x0, y0) + wsum4(x1, y1) + wsum4(x2, y2) + wsum4(x3, y3);
         }
+        for (; e < nv4; e += 32) acc += wsum4(__ldg(a4 + e), resid ? __ldg(b4 + e) : zero4);
         t = slo + 4 * nv4;
     }
     for (t += lane; t < shi; t += 32) acc += elem_weight(a, bq, t, resid);

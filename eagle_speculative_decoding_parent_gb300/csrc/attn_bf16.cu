@@ -94,71 +94,6 @@ __device__ __forceinline__ Group decode_group(const Params& p, int gi, int rank,
     return gr;
 }
 
-// ------------------------------------------------------------ cluster helpers
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void remote_arrive(uint64_t* bar, uint32_t rank) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                     map_rank(bar, rank))
-                 : "memory");
-}
-__device__ __forceinline__ void remote_st_u32(int* p, uint32_t rank, int v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_rank(p, rank)), "r"(v) : "memory");
-}
-__device__ __forceinline__ float4 remote_ld_f4(const float* p, uint32_t rank) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(map_rank(p, rank))
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ float2 remote_ld_f2(const float* p, uint32_t rank) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];"
-                 : "=f"(v.x), "=f"(v.y)
-                 : "r"(map_rank(p, rank))
-                 : "memory");
-    return v;
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait with cluster-scope acquire (peers write before arriving).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait_cluster(bar, parity)) {
-        if (globaltimer_ns() - t0 > TV_WAIT_NS) return false;
-    }
-    return true;
-}
-__device__ __forceinline__ void cluster_barrier_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 template <int D, int WM, int WK>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -623,38 +558,6 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-bool make_cache_map(CUtensorMap* map, const void* base, int d, int64_t rows) {
-    EncodeTiledFn enc = get_encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr size_t kSchedBytes = 256;  // two counters, padded
 
 void warp_grid(int M, int* WM, int* WK) {
@@ -675,6 +578,8 @@ size_t smem_bytes() {
 // Clusters resident at once for cluster size cs (0 if the launch cannot fit).
 template <int D, int WM, int WK>
 int resident_clusters(int cs, size_t smem) {
+    static int cache[17] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (cs >= 1 && cs <= 16 && cache[cs] >= 0) return cache[cs];
     auto kern = attn_bf16_kernel<D, WM, WK>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs);
@@ -690,8 +595,9 @@ int resident_clusters(int cs, size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
         cudaGetLastError();
-        return 0;
+        n = 0;
     }
+    if (cs >= 1 && cs <= 16) cache[cs] = n;
     return n;
 }
 
@@ -721,9 +627,13 @@ tv_status launch_typed(const AttnArgs& a, const CUtensorMap& km, const CUtensorM
                        Params prm) {
     auto kern = attn_bf16_kernel<D, WM, WK>;
     const size_t smem = smem_bytes<D, WM, WK>();
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return TV_ERR_CUDA;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return TV_ERR_CUDA;
+        attr_set = true;
+    }
     const int64_t tiles_max = ((int64_t)a.max_blocks * a.bs + KT - 1) / KT;
     int ncl = 0;
     const int cs = pick_cluster_size<D, WM, WK>(prm.groups, tiles_max, smem, &ncl);
@@ -761,6 +671,7 @@ tv_status launch_attn_bf16(const AttnArgs& a) {
     if (a.B == 0) return TV_OK;
     if (a.ws_bytes < kSchedBytes || a.ws == nullptr) return TV_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(a.ws) & 255) != 0) return TV_ERR_WORKSPACE;
+    if (attn_tc_applicable(a.N, a.Hq, a.Hkv, a.d)) return launch_attn_tc(a);
     const int64_t rows = (int64_t)a.num_blocks * a.Hkv * a.bs;
     if (rows >= (1LL << 31)) return TV_ERR_UNSUPPORTED;
     CUtensorMap km, vm;

@@ -1,0 +1,733 @@
+// tree_verify_attention, bfloat16 path on the 5th-generation tensor cores.
+//
+// Used when the packed row tile is a real dense contraction (more than 64
+// rows).  Same work decomposition as the warp-MMA kernel: a group is
+// (sequence, kv head, row tile); groups go dynamically to clusters of CS CTAs
+// that split the group's keys and merge through distributed shared memory.
+// A row tile holds npt = floor(128 / G) whole nodes (all G query heads of the
+// kv head for each), rows r = node * G + head, so one TMA box loads it.
+//
+// CTA roles (256 threads, one CTA per SM)
+//   warp 0   producer: Q tile (3-D TMA box), then 64-key K/V tiles (one 2-D
+//            box per 16-key page and 64-column half) through a 3-stage ring;
+//            in rank 0 also fetches group ids for the cluster.
+//   warp 1   MMA issuer (one thread): S = Q K^T into tensor memory (M=128,
+//            N=64, K=16 steps), O += P V (M=128, N=128, B operand N-major),
+//            completion signalled with tcgen05.commit.
+//   warp 2   allocates / frees 256 tensor-memory columns: S double buffer
+//            (2 x 64) and O (128).
+//   warps 4-7 softmax: thread i owns row i (tensor-memory lane i); reads S,
+//            applies scale and tree mask, keeps a running max that is only
+//            raised (and O rescaled in tensor memory) when it grows by more
+//            than 2^8, writes P (bf16) to shared memory for the PV product,
+//            and finally normalises O.
+#include <algorithm>
+
+#include "tv_device.cuh"
+#include "tv_internal.h"
+#include "tv_tc.cuh"
+
+namespace tv {
+
+namespace {
+
+constexpr int KT = 64;        // keys per tile
+constexpr int STAGES = 3;
+constexpr int GQ = 4;
+constexpr int THREADS = 256;
+constexpr int SOFTMAX_WARP0 = 4;
+constexpr int MAX_CS = 8;
+constexpr int D = 128;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_O = 128;         // O at columns 128..255, S buffers at 0 and 64
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_LOG2 = 8.0f;     // raise the running max only past 2^8 growth
+
+constexpr uint32_t IDESC_QK = idesc_bf16(128, KT, false);
+constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr int TILE_BYTES = KT * D * 2;                 // 16 KB: one K or V tile
+constexpr int OFF_RING = 0;                            // STAGES x (K, V)
+constexpr int OFF_Q = OFF_RING + STAGES * 2 * TILE_BYTES;
+constexpr int Q_BYTES = 128 * D * 2;                   // 32 KB
+constexpr int OFF_P = OFF_Q + Q_BYTES;                 // 2 x 16 KB
+constexpr int P_BYTES = 128 * KT * 2;
+constexpr int OFF_XO = OFF_P + 2 * P_BYTES;            // fp16 normalised O rows, 32 KB
+constexpr int XO_BYTES = 128 * D * 2;
+constexpr int OFF_XML = OFF_XO + XO_BYTES;             // (max, sum) per row
+constexpr int OFF_WTS = OFF_XML + 128 * 8;             // merge weights [128][MAX_CS]
+constexpr int OFF_BARS = OFF_WTS + 128 * MAX_CS * 4;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 1 + 2 * GQ + 2;
+constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;       // + alignment slack
+
+struct Params {
+    const int32_t* table;
+    const int32_t* prefix_lens;
+    const uint64_t* mask;
+    __nv_bfloat16* out;
+    int32_t* status;
+    int32_t* sched;
+    int max_blocks, B, N, Hq, Hkv, G, npt, bs, num_blocks, QT, groups;
+    float scale_log2;
+};
+
+struct Group {
+    int b, g, qt, P, L, t_lo, t_hi;
+    bool ok;
+};
+
+__device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
+    const int lane = threadIdx.x & 31;
+    bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
+    if (ok) {
+        const int nb = (P + p.N + p.bs - 1) / p.bs;
+        for (int j = lane; j < nb; j += 32) {
+            const int blk = p.table[(int64_t)b * p.max_blocks + j];
+            ok = ok && blk >= 0 && blk < p.num_blocks;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ Group decode_group(const Params& p, int gi, int rank, int cs) {
+    Group gr;
+    gr.qt = gi % p.QT;
+    gr.g = (gi / p.QT) % p.Hkv;
+    gr.b = gi / (p.QT * p.Hkv);
+    gr.P = p.prefix_lens[gr.b];
+    gr.L = gr.P + p.N;
+    gr.ok = seq_ok_warp(p, gr.b, gr.P);
+    const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
+    gr.t_lo = (int)((int64_t)T * rank / cs);
+    gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
+    return gr;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BARS);
+    uint64_t* kfull = bars;                   // [STAGES]
+    uint64_t* kempty = kfull + STAGES;        // [STAGES]
+    uint64_t* qfull = kempty + STAGES;
+    uint64_t* qempty = qfull + 1;
+    uint64_t* sfull = qempty + 1;             // [2]
+    uint64_t* sfree = sfull + 2;              // [2]
+    uint64_t* pfull = sfree + 2;              // [2]
+    uint64_t* pfree = pfull + 2;              // [2]
+    uint64_t* pvdone = pfree + 2;
+    uint64_t* ofree = pvdone + 1;
+    uint64_t* tailb = ofree + 1;
+    uint64_t* gq_full = tailb + 1;            // [GQ]
+    uint64_t* gq_empty = gq_full + GQ;        // [GQ]
+    uint64_t* xready = gq_empty + GQ;
+    uint64_t* xfree = xready + 1;
+    int* misc = reinterpret_cast<int*>(smem + OFF_MISC);
+    int* gq = misc;                           // [GQ]
+    uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(misc + GQ);
+    int* flags = misc + GQ + 1;               // [0] abort
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_rank(), cs = cluster_size();
+    const uint32_t sbase = smem_u32(smem);
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kempty[s], 1);
+        }
+        mbar_init(qfull, 1);
+        mbar_init(qempty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sfree[i], 4);
+            mbar_init(&pfull[i], 4);
+            mbar_init(&pfree[i], 1);
+        }
+        mbar_init(pvdone, 1);
+        mbar_init(ofree, 4);
+        mbar_init(tailb, 1);
+        for (int s = 0; s < GQ; ++s) {
+            mbar_init(&gq_full[s], 1);
+            mbar_init(&gq_empty[s], cs * 6);
+        }
+        mbar_init(xready, cs * 4);
+        mbar_init(xfree, cs * 4);
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_base_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_barrier_all();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_base_slot);
+
+    // group id k of this CTA (all roles walk the same sequence)
+    auto next_group = [&](uint32_t k, bool fetcher) -> int {
+        const int slot = k % GQ;
+        if (fetcher && lane == 0) {
+            const bool ok = mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u);
+            const int gi = ok ? atomicAdd(&p.sched[0], 1) : p.groups;
+            for (uint32_t r = 0; r < cs; ++r) {
+                remote_st_u32(&gq[slot], r, gi);
+                remote_arrive(&gq_full[slot], r);
+            }
+        }
+        const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&gq_full[slot], (k / GQ) & 1u));
+        const int gi = got ? *(volatile int*)&gq[slot] : p.groups;
+        __syncwarp();
+        if (lane == 0) remote_arrive(&gq_empty[slot], 0);
+        return gi;
+    };
+
+    if (warp == 0) {
+        // =========================== producer ===========================
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+        }
+        const uint64_t policy = (p.QT == 1) ? l2_policy_evict_first() : l2_policy_evict_normal();
+        uint32_t gt = 0, qi = 0, tail_phase = 0;
+        bool alive = true;
+        for (uint32_t k = 0; alive; ++k) {
+            const int gi = next_group(k, rank == 0);
+            if (gi >= p.groups) break;
+            const Group gr = decode_group(p, gi, rank, cs);
+            const int n = gr.t_hi - gr.t_lo;
+            if (n == 0) continue;
+            // Q tile: npt nodes x G heads x 128 columns
+            if (lane == 0) {
+                bool ok = mbar_wait(qempty, (qi & 1u) ^ 1u);
+                if (!ok) {
+                    flags[0] = 1;
+                    p.status[gr.b] = TV_ERR_TIMEOUT;
+                }
+                const uint32_t qbytes = 2u * 64u * (uint32_t)(p.G * p.npt) * 2u;
+                mbar_arrive_expect_tx(qfull, qbytes);
+                const int node0 = gr.b * p.N + gr.qt * p.npt;
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d(smem + OFF_Q + hf * (128 * 128), &qmap, qfull, hf * 64, gr.g * p.G,
+                                node0);
+            }
+            ++qi;
+            for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
+                const int s = gt % STAGES;
+                const uint32_t ph = (gt / STAGES) & 1u;
+                bool freed = !*(volatile int*)&flags[0];
+                if (lane == 0 && freed) freed = mbar_wait(&kempty[s], ph ^ 1u);
+                freed = __shfl_sync(0xffffffffu, freed, 0);
+                if (!freed) {
+                    if (lane == 0) {
+                        flags[0] = 1;
+                        p.status[gr.b] = TV_ERR_TIMEOUT;
+                    }
+                    alive = false;
+                    break;
+                }
+                const int t0 = t * KT;
+                const int nv = min(KT, gr.L - t0);
+                const int pages = (nv + 15) >> 4;
+                const uint32_t bytes = (uint32_t)pages * 16u * D * 2u * 2u;
+                const bool tail = nv < KT;
+                uint64_t* bar = tail ? tailb : &kfull[s];
+                uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
+                uint8_t* vt = kt + TILE_BYTES;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, bytes);
+                    for (int pg = 0; pg < pages; ++pg) {
+                        const int tk = t0 + pg * 16;
+                        const int blk = p.table[(int64_t)gr.b * p.max_blocks + tk / p.bs];
+                        const int y = (blk * p.Hkv + gr.g) * p.bs + (tk % p.bs);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            tma_load_2d(kt + hf * (KT * 128) + pg * 2048, &kmap, bar, hf * 64, y, policy);
+                            tma_load_2d(vt + hf * (KT * 128) + pg * 2048, &vmap, bar, hf * 64, y, policy);
+                        }
+                    }
+                }
+                if (tail) {
+                    const bool landed = __all_sync(0xffffffffu, mbar_wait(tailb, tail_phase));
+                    tail_phase ^= 1u;
+                    if (!landed) {
+                        if (lane == 0) {
+                            flags[0] = 1;
+                            p.status[gr.b] = TV_ERR_TIMEOUT;
+                        }
+                        alive = false;
+                        break;
+                    }
+                    // rows past the sequence end may hold anything: zero V there (K rows are masked)
+                    const int zrows = KT - nv;
+                    for (int e = lane; e < 2 * zrows * 8; e += 32) {
+                        const int hf = e / (zrows * 8);
+                        const int r = nv + (e / 8) % zrows;
+                        const int ch = e % 8;
+                        *reinterpret_cast<uint4*>(vt + hf * (KT * 128) + r * 128 + ch * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();  // the tensor core reads V through the async proxy
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kfull[s]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // =========================== MMA issuer ===========================
+        uint32_t gt = 0, qi = 0, og = 0;
+        const uint32_t tS = tmem, tO = tmem + TMEM_O;
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+        };
+        auto do_pv = [&](uint32_t t, bool first) -> bool {
+            const int pb = t & 1;
+            if (!wait_all(&pfull[pb], (t >> 1) & 1u)) return false;
+            if (first && og > 0 && !wait_all(ofree, (og - 1) & 1u)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const int s = t % STAGES;
+                const uint32_t pa = sbase + OFF_P + pb * P_BYTES;
+                const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < KT / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(pa + kk * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
+                    tc_mma_bf16(tO, ad, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                }
+                tc_commit(&kempty[s]);
+                tc_commit(&pfree[pb]);
+                tc_commit(pvdone);
+            }
+            __syncwarp();
+            return true;
+        };
+        bool alive = true;
+        for (uint32_t k = 0; alive; ++k) {
+            const int gi = next_group(k, false);
+            if (gi >= p.groups) break;
+            const Group gr = decode_group(p, gi, rank, cs);
+            const int n = gr.t_hi - gr.t_lo;
+            if (n == 0) continue;
+            if (!wait_all(qfull, qi & 1u)) { alive = false; break; }
+            ++qi;
+            const uint32_t first_tile = gt;
+            for (int j = 0; j < n; ++j, ++gt) {
+                const int s = gt % STAGES, sb = gt & 1;
+                if (!wait_all(&kfull[s], (gt / STAGES) & 1u) ||
+                    !wait_all(&sfree[sb], ((gt >> 1) & 1u) ^ 1u)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t qa = sbase + OFF_Q;
+                    const uint32_t ka = sbase + OFF_RING + s * 2 * TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * (KT * 128) + (kk & 3) * 32, 16, 1024);
+                        tc_mma_bf16(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&sfull[sb]);
+                    if (j == n - 1) tc_commit(qempty);
+                }
+                __syncwarp();
+                if (j > 0 && !do_pv(gt - 1, gt - 1 == first_tile)) {
+                    alive = false;
+                    break;
+                }
+            }
+            if (!alive) break;
+            if (!do_pv(gt - 1, gt - 1 == first_tile)) break;
+            ++og;
+        }
+        if (!alive && lane == 0) flags[0] = 1;
+    } else if (warp >= SOFTMAX_WARP0) {
+        // ============================= softmax =============================
+        const int row = tid - SOFTMAX_WARP0 * 32;           // tensor-memory lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp - SOFTMAX_WARP0)) << 16;
+        const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + TMEM_O;
+        uint8_t* xo = smem + OFF_XO;
+        float2* xml = reinterpret_cast<float2*>(smem + OFF_XML);
+        float* wts = reinterpret_cast<float*>(smem + OFF_WTS);
+        uint32_t gt = 0, merges = 0;
+        uint32_t pv_seen = 0;  // PV completions consumed, strictly in order (parity waits)
+        bool alive = true;
+        // waits until the PV products of tiles < upto are complete, one phase at a time
+        auto consume_pv = [&](uint32_t upto) -> bool {
+            bool ok = true;
+            while (ok && pv_seen < upto) {
+                ok = __all_sync(0xffffffffu, mbar_wait(pvdone, pv_seen & 1u));
+                ++pv_seen;
+            }
+            return ok;
+        };
+        for (uint32_t k = 0;; ++k) {
+            const int gi = next_group(k, false);
+            if (gi >= p.groups) break;
+            const Group gr = decode_group(p, gi, rank, cs);
+            if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
+                p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
+            const int n = gr.t_hi - gr.t_lo;
+            const int node_l = row / p.G, head = row % p.G;
+            const int node = gr.qt * p.npt + node_l;
+            const bool valid = (node_l < p.npt) && (node < p.N);
+            const uint64_t nmask = (p.N >= 64) ? ~0ull : ((1ull << p.N) - 1);
+            const uint64_t mk = valid ? (p.mask[(int64_t)gr.b * p.N + node] & nmask) : 0ull;
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < n && alive; ++j, ++gt) {
+                const int sb = gt & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&sfull[sb], (gt >> 1) & 1u))) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+                float sv[KT];
+                {
+                    uint32_t r[32];
+                    tmem_ld32(tS + sb * KT, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
+                    tmem_ld32(tS + sb * KT + 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sfree[sb]);
+                const int t0 = (gr.t_lo + j) * KT;
+                float tmax = -INFINITY;
+                if (t0 + KT > gr.P) {
+#pragma unroll
+                    for (int c = 0; c < KT; ++c) {
+                        const int t = t0 + c;
+                        const bool vis = (t < gr.P) ||
+                                         (t < gr.L && ((mk >> (t - gr.P)) & 1ull));
+                        sv[c] = vis ? sv[c] * p.scale_log2 : -INFINITY;
+                        tmax = fmaxf(tmax, sv[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < KT; ++c) {
+                        sv[c] *= p.scale_log2;
+                        tmax = fmaxf(tmax, sv[c]);
+                    }
+                }
+                const float m_new = fmaxf(m_used, tmax);
+                const bool need = (m_used == -INFINITY) ? (m_new > -INFINITY)
+                                                        : (m_new > m_used + RESCALE_LOG2);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float f = (need && m_used > -INFINITY) ? exp2f(m_used - m_new) : 1.f;
+                    if (j > 0) {
+                        // O holds the products of earlier tiles: rescale it once they are done
+                        if (!consume_pv(gt)) {
+                            alive = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t r[32];
+                            tmem_ld32(tO + c, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                            tmem_st32(tO + c, r);
+                        }
+                        tmem_wait_st();
+                    }
+                    l *= f;
+                    if (need) m_used = m_new;
+                }
+                const float base = (m_used == -INFINITY) ? 0.f : m_used;
+                uint32_t pk[KT / 2];
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < KT; c += 2) {
+                    const float a = exp2f(sv[c] - base), b2 = exp2f(sv[c + 1] - base);
+                    rs += a + b2;
+                    pk[c / 2] = pack_bf16x2(a, b2);
+                }
+                l += rs;
+                // P row -> shared memory (K-major, 128-byte swizzle) once its buffer is free
+                const int pb = gt & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&pfree[pb], ((gt >> 1) & 1u) ^ 1u))) {
+                    alive = false;
+                    break;
+                }
+                uint8_t* prow = smem + OFF_P + pb * P_BYTES + row * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                fence_proxy_async_smem();
+                // keep PV completions consumed in order: the previous tile's product
+                // must be done before this tile's P is published
+                if (!consume_pv(gt)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&pfull[pb]);
+            }
+            if (!alive) break;
+            // ---- epilogue: O / l
+            float o_inv = (l > 0.f) ? 1.f / l : 0.f;
+            __nv_bfloat16* orow = nullptr;
+            if (valid)
+                orow = p.out + (((int64_t)gr.b * p.N + node) * p.Hq + gr.g * p.G + head) * D;
+            if (cs > 1 && merges > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait_cluster(xfree, (merges - 1) & 1u))) {
+                alive = false;
+                break;
+            }
+            if (n > 0) {
+                if (!consume_pv(gt)) {
+                    alive = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                if (n > 0) {
+                    tmem_ld32(tO + c, r);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = 0u;
+                }
+                if (cs == 1) {
+                    if (valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(r[e]) * o_inv, __uint_as_float(r[e + 1]) * o_inv);
+                            v.y = pack_bf16x2(__uint_as_float(r[e + 2]) * o_inv, __uint_as_float(r[e + 3]) * o_inv);
+                            v.z = pack_bf16x2(__uint_as_float(r[e + 4]) * o_inv, __uint_as_float(r[e + 5]) * o_inv);
+                            v.w = pack_bf16x2(__uint_as_float(r[e + 6]) * o_inv, __uint_as_float(r[e + 7]) * o_inv);
+                            *reinterpret_cast<uint4*>(orow + c + e) = v;
+                        }
+                    }
+                } else {
+                    // normalised row, fp16, into this CTA's exchange buffer (16-byte chunks)
+                    uint8_t* xr = xo + row * (D * 2);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        __half2 h0 = __floats2half2_rn(__uint_as_float(r[e]) * o_inv, __uint_as_float(r[e + 1]) * o_inv);
+                        __half2 h1 = __floats2half2_rn(__uint_as_float(r[e + 2]) * o_inv, __uint_as_float(r[e + 3]) * o_inv);
+                        __half2 h2 = __floats2half2_rn(__uint_as_float(r[e + 4]) * o_inv, __uint_as_float(r[e + 5]) * o_inv);
+                        __half2 h3 = __floats2half2_rn(__uint_as_float(r[e + 6]) * o_inv, __uint_as_float(r[e + 7]) * o_inv);
+                        uint4 v;
+                        v.x = *reinterpret_cast<uint32_t*>(&h0);
+                        v.y = *reinterpret_cast<uint32_t*>(&h1);
+                        v.z = *reinterpret_cast<uint32_t*>(&h2);
+                        v.w = *reinterpret_cast<uint32_t*>(&h3);
+                        *reinterpret_cast<uint4*>(xr + (c + e) * 2) = v;
+                    }
+                }
+            }
+            if (n > 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ofree);  // O may be overwritten by the next group
+            }
+            if (cs == 1) continue;
+            // ---- cluster merge: this CTA finishes rows [rank*128/cs, (rank+1)*128/cs)
+            xml[row] = make_float2(m_used, l);
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            named_bar_sync(2, 128);
+            if (lane == 0)
+                for (uint32_t r = 0; r < cs; ++r) remote_arrive(xready, r);
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(xready, merges & 1u))) {
+                alive = false;
+                break;
+            }
+            const int rows_per = 128 / (int)cs;
+            const int rb = (int)rank * rows_per;
+            if (row < rows_per) {
+                const int lr = rb + row;
+                float mx = -INFINITY;
+                for (uint32_t c = 0; c < cs; ++c) mx = fmaxf(mx, remote_ld_f2(reinterpret_cast<const float*>(&xml[lr]), c).x);
+                const float bz = (mx == -INFINITY) ? 0.f : mx;
+                float den = 0.f;
+                for (uint32_t c = 0; c < cs; ++c) {
+                    const float2 ml = remote_ld_f2(reinterpret_cast<const float*>(&xml[lr]), c);
+                    const float w = exp2f(ml.x - bz) * ml.y;
+                    wts[lr * MAX_CS + c] = w;
+                    den += w;
+                }
+                const float inv = (den > 0.f) ? 1.f / den : 0.f;
+                for (uint32_t c = 0; c < cs; ++c) wts[lr * MAX_CS + c] *= inv;
+            }
+            named_bar_sync(2, 128);
+            for (int e = row; e < rows_per * (D / 8); e += 128) {
+                const int lr = rb + e / (D / 8);
+                const int c8 = (e % (D / 8)) * 8;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (uint32_t c = 0; c < cs; ++c) {
+                    const float w = wts[lr * MAX_CS + c];
+                    const uint4 v = remote_ld_u4(xo + lr * (D * 2) + c8 * 2, c);
+                    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 f2 = __half22float2(h[q]);
+                        acc[2 * q] += w * f2.x;
+                        acc[2 * q + 1] += w * f2.y;
+                    }
+                }
+                const int nl = lr / p.G, hd = lr % p.G;
+                const int nd = gr.qt * p.npt + nl;
+                if (nl < p.npt && nd < p.N) {
+                    __nv_bfloat16* dst = p.out + (((int64_t)gr.b * p.N + nd) * p.Hq + gr.g * p.G + hd) * D + c8;
+                    uint4 v;
+                    v.x = pack_bf16x2(acc[0], acc[1]);
+                    v.y = pack_bf16x2(acc[2], acc[3]);
+                    v.z = pack_bf16x2(acc[4], acc[5]);
+                    v.w = pack_bf16x2(acc[6], acc[7]);
+                    *reinterpret_cast<uint4*>(dst) = v;
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                for (uint32_t r = 0; r < cs; ++r) remote_arrive(xfree, r);
+            ++merges;
+        }
+        if (!alive && lane == 0) {
+            flags[0] = 1;
+        }
+        if (cs > 1 && merges > 0) mbar_wait_cluster(xfree, (merges - 1) & 1u);
+        __syncwarp();
+    }
+    // warps 2-3 (and every role once done) meet here
+    tc_fence_before();
+    cluster_barrier_all();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
+    if (tid == 0) {
+        __threadfence();
+        const int done = atomicAdd(&p.sched[1], 1);
+        if (done == (int)gridDim.x - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+        }
+    }
+}
+
+
+// ---------------------------------------------------------------- host side
+int resident_clusters_tc(int cs) {
+    static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (cs < 1 || cs > 8) return 0;
+    if (cache[cs] >= 0) return cache[cs];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = cs;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[cs] = n;
+    return n;
+}
+
+}  // namespace
+
+bool attn_tc_applicable(int N, int Hq, int Hkv, int d) {
+    const int G = Hq / Hkv;
+    return d == D && G <= 128 && N * G > 64;
+}
+
+tv_status launch_attn_tc(const AttnArgs& a) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
+            return TV_ERR_CUDA;
+        attr_set = true;
+    }
+    const int G = a.Hq / a.Hkv;
+    const int npt = 128 / G;
+    const int64_t rows = (int64_t)a.num_blocks * a.Hkv * a.bs;
+    if (rows >= (1LL << 31)) return TV_ERR_UNSUPPORTED;
+    CUtensorMap qm, km, vm;
+    if (!make_q_map(&qm, a.q, D, a.Hq, (int64_t)a.B * a.N, G, npt) ||
+        !make_cache_map(&km, a.k_cache, D, rows) || !make_cache_map(&vm, a.v_cache, D, rows))
+        return TV_ERR_CUDA;
+    Params prm{};
+    prm.table = a.block_table;
+    prm.prefix_lens = a.prefix_lens;
+    prm.mask = a.mask;
+    prm.out = static_cast<__nv_bfloat16*>(a.out);
+    prm.status = a.status;
+    prm.sched = static_cast<int32_t*>(a.ws);
+    prm.max_blocks = a.max_blocks;
+    prm.B = a.B;
+    prm.N = a.N;
+    prm.Hq = a.Hq;
+    prm.Hkv = a.Hkv;
+    prm.G = G;
+    prm.npt = npt;
+    prm.bs = a.bs;
+    prm.num_blocks = a.num_blocks;
+    prm.QT = (a.N + npt - 1) / npt;
+    const int64_t groups = (int64_t)a.B * a.Hkv * prm.QT;
+    if (groups >= (1LL << 30)) return TV_ERR_UNSUPPORTED;
+    prm.groups = (int)groups;
+    prm.scale_log2 = a.scale * LOG2E;
+    // cluster size: minimise rounds x (tiles per CTA + one tile of merge cost)
+    const int64_t tiles_max = ((int64_t)a.max_blocks * a.bs + KT - 1) / KT;
+    int best_cs = 1, best_ncl = 0;
+    double best = 1e300;
+    for (int cs = 1; cs <= MAX_CS; cs *= 2) {
+        if (cs > 1 && tiles_max < 2 * cs) break;
+        const int ncl = resident_clusters_tc(cs);
+        if (ncl <= 0) continue;
+        const int64_t rounds = (groups + ncl - 1) / ncl;
+        const double cost = (double)rounds * ((double)tiles_max / cs + (cs > 1 ? 1.0 : 0.0));
+        if (cost < best * 0.97) {
+            best = cost;
+            best_cs = cs;
+            best_ncl = ncl;
+        }
+    }
+    if (best_ncl <= 0) return TV_ERR_CUDA;
+    const int clusters = (int)std::min<int64_t>(best_ncl, groups);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(clusters * best_cs));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = best_cs;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, qm, km, vm, prm) == cudaSuccess ? TV_OK
+                                                                                     : TV_ERR_CUDA;
+}
+
+}  // namespace tv

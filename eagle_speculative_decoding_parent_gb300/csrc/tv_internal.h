@@ -1,6 +1,7 @@
 // Host-side interfaces between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,10 +31,20 @@ struct AttnArgs {
     cudaStream_t stream;
 };
 
+// TMA descriptors (cuTensorMapEncodeTiled through the runtime's driver entry point).
+// K or V cache viewed as rows of d bf16 elements: box 64 columns x 16 rows, 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* base, int d, int64_t rows);
+// Q [B*N][Hq][d] bf16: box 64 columns x G heads x npt nodes, 128-byte swizzle.
+bool make_q_map(CUtensorMap* map, const void* base, int d, int Hq, int64_t nodes, int G,
+                int npt);
+
 tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask, int32_t* depth,
                            int32_t* status, cudaStream_t stream);
 tv_status launch_attn_f32(const AttnArgs& a);
 size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs);
+// tensor-core (tcgen05) variant for row tiles wider than 64 rows; same workspace
+bool attn_tc_applicable(int N, int Hq, int Hkv, int d);
+tv_status launch_attn_tc(const AttnArgs& a);
 // Leading bytes of that workspace that must be zero when a call starts.
 size_t attn_bf16_workspace_zeroed_prefix(int B, int N, int Hq, int Hkv, int d, int max_blocks,
                                          int bs);
