@@ -173,6 +173,11 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             if (lane == 0) remote_arrive(&gq_empty[slot], 0);
             if (gi >= p.groups) break;
             const Group gr = decode_group(p, gi, rank, cs);
+            // block id of the page holding logical position tk (0 past the sequence end)
+            auto page_block = [&](int tk) -> int {
+                return (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+            };
+            int blk_cur = (gr.t_lo < gr.t_hi && lane < KT / 16) ? page_block(gr.t_lo * KT + lane * 16) : 0;
             for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
                 const int s = gt % STAGES;
                 const uint32_t ph = (gt / STAGES) & 1u;
@@ -195,19 +200,21 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 uint64_t* bar = tail ? tail_bar : &full_bar[s];
                 uint8_t* kt = ring + s * LY::STAGE_BYTES;
                 uint8_t* vt = kt + LY::TILE_BYTES;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar, bytes);
-                    for (int pg = 0; pg < pages; ++pg) {
-                        const int tk = t0 + pg * 16;
-                        const int blk = p.table[(int64_t)gr.b * p.max_blocks + tk / p.bs];
-                        const int y = (blk * p.Hkv + gr.g) * p.bs + (tk % p.bs);
+                // one lane per 16-key page: lane 0 posts the byte count, then every
+                // page's lane issues its own copies with the block id it already holds
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+                __syncwarp();
+                if (lane < pages) {
+                    const int tk = t0 + lane * 16;
+                    const int y = (blk_cur * p.Hkv + gr.g) * p.bs + (tk % p.bs);
 #pragma unroll
-                        for (int hf = 0; hf < D / 64; ++hf) {
-                            tma_load_2d(kt + hf * (KT * 128) + pg * 2048, &kmap, bar, hf * 64, y, policy);
-                            tma_load_2d(vt + hf * (KT * 128) + pg * 2048, &vmap, bar, hf * 64, y, policy);
-                        }
+                    for (int hf = 0; hf < D / 64; ++hf) {
+                        tma_load_2d(kt + hf * (KT * 128) + lane * 2048, &kmap, bar, hf * 64, y, policy);
+                        tma_load_2d(vt + hf * (KT * 128) + lane * 2048, &vmap, bar, hf * 64, y, policy);
                     }
                 }
+                // block ids for the next tile, one page per lane, while this one is in flight
+                if (t + 1 < gr.t_hi && lane < KT / 16) blk_cur = page_block((t + 1) * KT + lane * 16);
                 if (tail) {
                     // wait for the partial tile, zero the V rows past the sequence end
                     // (they may hold anything), then publish the stage

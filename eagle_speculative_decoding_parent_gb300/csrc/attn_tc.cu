@@ -219,6 +219,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                 node0);
             }
             ++qi;
+            // block id of the page holding logical position tk (0 past the sequence end)
+            auto page_block = [&](int tk) -> int {
+                return (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+            };
+            int blk_cur = (gr.t_lo < gr.t_hi && lane < KT / 16) ? page_block(gr.t_lo * KT + lane * 16) : 0;
             for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
                 const int s = gt % STAGES;
                 const uint32_t ph = (gt / STAGES) & 1u;
@@ -241,19 +246,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 uint64_t* bar = tail ? tailb : &kfull[s];
                 uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
                 uint8_t* vt = kt + TILE_BYTES;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar, bytes);
-                    for (int pg = 0; pg < pages; ++pg) {
-                        const int tk = t0 + pg * 16;
-                        const int blk = p.table[(int64_t)gr.b * p.max_blocks + tk / p.bs];
-                        const int y = (blk * p.Hkv + gr.g) * p.bs + (tk % p.bs);
+                // one lane per 16-key page: lane 0 posts the byte count, then every
+                // page's lane issues its own copies with the block id it already holds
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+                __syncwarp();
+                if (lane < pages) {
+                    const int tk = t0 + lane * 16;
+                    const int y = (blk_cur * p.Hkv + gr.g) * p.bs + (tk % p.bs);
 #pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            tma_load_2d(kt + hf * (KT * 128) + pg * 2048, &kmap, bar, hf * 64, y, policy);
-                            tma_load_2d(vt + hf * (KT * 128) + pg * 2048, &vmap, bar, hf * 64, y, policy);
-                        }
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tma_load_2d(kt + hf * (KT * 128) + lane * 2048, &kmap, bar, hf * 64, y, policy);
+                        tma_load_2d(vt + hf * (KT * 128) + lane * 2048, &vmap, bar, hf * 64, y, policy);
                     }
                 }
+                // block ids for the next tile, one page per lane, while this one is in flight
+                if (t + 1 < gr.t_hi && lane < KT / 16) blk_cur = page_block((t + 1) * KT + lane * 16);
                 if (tail) {
                     const bool landed = __all_sync(0xffffffffu, mbar_wait(tailb, tail_phase));
                     tail_phase ^= 1u;
@@ -392,15 +399,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 tc_fence_after();
                 float sv[KT];
                 {
-                    uint32_t r[32];
+                    uint32_t r[32], r2[32];
                     tmem_ld32(tS + sb * KT, r);
+                    tmem_ld32(tS + sb * KT + 32, r2);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r[c]);
-                    tmem_ld32(tS + sb * KT + 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r[c]);
+                    for (int c = 0; c < 32; ++c) {
+                        sv[c] = __uint_as_float(r[c]);
+                        sv[32 + c] = __uint_as_float(r2[c]);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -413,16 +420,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const int t = t0 + c;
                         const bool vis = (t < gr.P) ||
                                          (t < gr.L && ((mk >> (t - gr.P)) & 1ull));
-                        sv[c] = vis ? sv[c] * p.scale_log2 : -INFINITY;
+                        sv[c] = vis ? sv[c] : -INFINITY;
                         tmax = fmaxf(tmax, sv[c]);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < KT; ++c) {
-                        sv[c] *= p.scale_log2;
-                        tmax = fmaxf(tmax, sv[c]);
-                    }
+                    for (int c = 0; c < KT; ++c) tmax = fmaxf(tmax, sv[c]);
                 }
+                tmax *= p.scale_log2;  // scores stay unscaled; the scale is folded into the exponent
                 const float m_new = fmaxf(m_used, tmax);
                 const bool need = (m_used == -INFINITY) ? (m_new > -INFINITY)
                                                         : (m_new > m_used + RESCALE_LOG2);
@@ -449,12 +454,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     l *= f;
                     if (need) m_used = m_new;
                 }
-                const float base = (m_used == -INFINITY) ? 0.f : m_used;
+                const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
+                const float csc = p.scale_log2;
                 uint32_t pk[KT / 2];
                 float rs = 0.f;
 #pragma unroll
                 for (int c = 0; c < KT; c += 2) {
-                    const float a = exp2f(sv[c] - base), b2 = exp2f(sv[c + 1] - base);
+                    const float a = ex2_approx(fmaf(sv[c], csc, nbase));
+                    const float b2 = ex2_approx(fmaf(sv[c + 1], csc, nbase));
                     rs += a + b2;
                     pk[c / 2] = pack_bf16x2(a, b2);
                 }
