@@ -302,7 +302,9 @@ def run_ours(args):
         one_step()
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # timed region: the four kernels of each step back to back (no events
+    # between them, so each kernel may start while the previous one drains)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -315,16 +317,26 @@ def run_ours(args):
         # keep the GPU busy while the host enqueues the step, so the event
         # intervals hold device time only (no host launch gaps)
         torch.cuda._sleep(SLEEP_CYCLES)
-        one_step(evs[k])
+        evs[k][0].record(stream)
+        one_step()
+        evs[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    per = np.array([[evs[k][j].elapsed_time(evs[k][j + 1]) for j in range(4)]
-                    for k in range(args.steps)])  # ms: mask, attn, accept, compact
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)])
     total_ms = float(step_ms.sum())
+
+    # per-kernel durations (events between the kernels), same inputs and flush
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        torch.cuda._sleep(SLEEP_CYCLES)
+        one_step(kev[k])
+    torch.cuda.synchronize()
+    per = np.array([[kev[k][j].elapsed_time(kev[k][j + 1]) for j in range(4)]
+                    for k in range(args.steps)])  # ms: mask, attn, accept, compact
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)

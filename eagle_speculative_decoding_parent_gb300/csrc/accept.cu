@@ -298,6 +298,8 @@ accept_greedy_kernel(AccParams p) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.x / C;
     __shared__ int spar[64], stok[64], sam[64];
     __shared__ ArgBest exch[2][64];
@@ -388,6 +390,8 @@ accept_rowscan_kernel(AccParams p, int32_t* __restrict__ am_ws, int32_t* __restr
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
+    pdl_launch_dependents();
+    pdl_wait();
     const int cl = blockIdx.x / S;
     const int N = p.N;
     const int b = cl / N, row = cl % N;
@@ -468,6 +472,8 @@ accept_stochastic_kernel(AccParams p) {
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
+    pdl_launch_dependents();
+    pdl_wait();
     const int b = blockIdx.x / C;
     __shared__ int spar[64], stok[64];
     __shared__ uint64_t wsum[ACC_WARPS];
@@ -653,18 +659,8 @@ tv_status launch_accept(const AcceptArgs& a) {
     if (C > cmax) C = cmax;
     while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
     if (units * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * C));
-    cfg.blockDim = dim3(ACC_THREADS);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = C;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
+    LaunchCfg lc(dim3((unsigned)(units * C)), dim3(ACC_THREADS), 0, a.stream, (unsigned)C);
+    const cudaLaunchConfig_t& cfg = lc.cfg;
     cudaError_t e;
     if (a.mode == TV_ACCEPT_GREEDY && rowscan) {
         int32_t* am = static_cast<int32_t*>(a.ws);

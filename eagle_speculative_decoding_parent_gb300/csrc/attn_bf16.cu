@@ -143,8 +143,10 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         flags[0] = 0;
         fence_mbar_init();
     }
+    pdl_launch_dependents();
     // every CTA of the cluster has initialised its barriers before any remote arrive
     cluster_barrier_all();
+    pdl_wait();  // everything above touched only shared memory
 
     if (warp == CONSUMER_WARPS) {
         // =========================== producer ===========================
@@ -646,19 +648,8 @@ tv_status launch_typed(const AttnArgs& a, const CUtensorMap& km, const CUtensorM
     const int cs = pick_cluster_size<D, WM, WK>(prm.groups, tiles_max, smem, &ncl);
     if (ncl <= 0) return TV_ERR_CUDA;
     const int clusters = std::min<int64_t>(ncl, prm.groups);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(clusters * cs));
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = cs;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, km, vm, prm) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    LaunchCfg lc(dim3((unsigned)(clusters * cs)), dim3(THREADS), smem, a.stream, (unsigned)cs);
+    return cudaLaunchKernelEx(&lc.cfg, kern, km, vm, prm) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
 }  // namespace

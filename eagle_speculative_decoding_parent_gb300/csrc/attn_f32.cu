@@ -18,6 +18,8 @@ attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
     constexpr int D = DPL * 32;
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    pdl_launch_dependents();
+    pdl_wait();
     if (gw >= (int64_t)B * N * Hq) return;
     const int h = (int)(gw % Hq);
     const int64_t bi = gw / Hq;
@@ -115,12 +117,14 @@ tv_status launch_attn_f32(const AttnArgs& a) {
     const int threads = 128;
     const int64_t blocks = (warps * 32 + threads - 1) / threads;
     if (blocks > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+    LaunchCfg lc(dim3((unsigned)blocks), dim3(threads), 0, a.stream);
+    cudaError_t e = cudaSuccess;
 #define TV_F32_CASE(DPL)                                                                       \
     case DPL:                                                                                  \
-        attn_f32_kernel<DPL><<<(unsigned)blocks, threads, 0, a.stream>>>(                     \
-            (const float*)a.q, (const float*)a.k_cache, (const float*)a.v_cache,               \
-            a.block_table, a.max_blocks, a.prefix_lens, a.mask, a.B, a.N, a.Hq, a.Hkv, a.bs,   \
-            a.num_blocks, a.scale, (float*)a.out, a.status);                                   \
+        e = cudaLaunchKernelEx(&lc.cfg, attn_f32_kernel<DPL>, (const float*)a.q,              \
+                               (const float*)a.k_cache, (const float*)a.v_cache, a.block_table, \
+                               a.max_blocks, a.prefix_lens, a.mask, a.B, a.N, a.Hq, a.Hkv,      \
+                               a.bs, a.num_blocks, a.scale, (float*)a.out, a.status);           \
         break;
     switch (a.d / 32) {
         TV_F32_CASE(1)
@@ -135,7 +139,7 @@ tv_status launch_attn_f32(const AttnArgs& a) {
             return TV_ERR_UNSUPPORTED;
     }
 #undef TV_F32_CASE
-    return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
 }  // namespace tv

@@ -32,14 +32,15 @@ namespace tv {
 namespace {
 
 constexpr int KT = 64;        // keys per tile
-constexpr int STAGES = 3;
+constexpr int STAGES = 4;
 constexpr int GQ = 4;
 constexpr int THREADS = 256;
 constexpr int SOFTMAX_WARP0 = 4;
 constexpr int MAX_CS = 8;
 constexpr int D = 128;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = 128;         // O at columns 128..255, S buffers at 0 and 64
+constexpr uint32_t TMEM_P = 256;         // P buffers (packed bf16 pairs) at 256 and 288
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_LOG2 = 8.0f;     // raise the running max only past 2^8 growth
 
@@ -51,9 +52,7 @@ constexpr int TILE_BYTES = KT * D * 2;                 // 16 KB: one K or V tile
 constexpr int OFF_RING = 0;                            // STAGES x (K, V)
 constexpr int OFF_Q = OFF_RING + STAGES * 2 * TILE_BYTES;
 constexpr int Q_BYTES = 128 * D * 2;                   // 32 KB
-constexpr int OFF_P = OFF_Q + Q_BYTES;                 // 2 x 16 KB
-constexpr int P_BYTES = 128 * KT * 2;
-constexpr int OFF_XO = OFF_P + 2 * P_BYTES;            // fp16 normalised O rows, 32 KB
+constexpr int OFF_XO = OFF_Q + Q_BYTES;                // fp16 normalised O rows, 32 KB
 constexpr int XO_BYTES = 128 * D * 2;
 constexpr int OFF_XML = OFF_XO + XO_BYTES;             // (max, sum) per row
 constexpr int OFF_WTS = OFF_XML + 128 * 8;             // merge weights [128][MAX_CS]
@@ -135,6 +134,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), cs = cluster_size();
     const uint32_t sbase = smem_u32(smem);
+    pdl_launch_dependents();
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -168,6 +168,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_before();
     cluster_barrier_all();
     tc_fence_after();
+    pdl_wait();  // everything above touched only shared memory and TMEM
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_base_slot);
 
     // group id k of this CTA (all roles walk the same sequence)
@@ -301,13 +302,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tc_fence_after();
             if (lane == 0) {
                 const int s = t % STAGES;
-                const uint32_t pa = sbase + OFF_P + pb * P_BYTES;
+                const uint32_t pa = tmem + TMEM_P + pb * (KT / 2);
                 const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(pa + kk * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
-                    tc_mma_bf16(tO, ad, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                    tc_mma_bf16_ts(tO, pa + kk * 8, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
                 }
                 tc_commit(&kempty[s]);
                 tc_commit(&pfree[pb]);
@@ -466,18 +466,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     pk[c / 2] = pack_bf16x2(a, b2);
                 }
                 l += rs;
-                // P row -> shared memory (K-major, 128-byte swizzle) once its buffer is free
+                // P row -> tensor memory (this thread's lane) once its buffer is free
                 const int pb = gt & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&pfree[pb], ((gt >> 1) & 1u) ^ 1u))) {
                     alive = false;
                     break;
                 }
-                uint8_t* prow = smem + OFF_P + pb * P_BYTES + row * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                fence_proxy_async_smem();
+                tmem_st32(tmem + lane_off + TMEM_P + pb * (KT / 2), pk);
+                tmem_wait_st();
                 // keep PV completions consumed in order: the previous tile's product
                 // must be done before this tile's P is published
                 if (!consume_pv(gt)) {
@@ -721,20 +717,11 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     }
     if (best_ncl <= 0) return TV_ERR_CUDA;
     const int clusters = (int)std::min<int64_t>(best_ncl, groups);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(clusters * best_cs));
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = best_cs;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel, qm, km, vm, prm) == cudaSuccess ? TV_OK
-                                                                                     : TV_ERR_CUDA;
+    LaunchCfg lc(dim3((unsigned)(clusters * best_cs)), dim3(THREADS), SMEM_BYTES, a.stream,
+                 (unsigned)best_cs);
+    return cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel, qm, km, vm, prm) == cudaSuccess
+               ? TV_OK
+               : TV_ERR_CUDA;
 }
 
 }  // namespace tv

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(CP_THREADS) kv_compact_kernel(CpParams p) {
     const int g = blockIdx.x, b = blockIdx.y;
     const int layer = blockIdx.z >> 1, which = blockIdx.z & 1;
     const int tid = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
     const int P = p.prefix_lens[b];
     const int A = p.accept_len[b];
     if (tid == 0) sok = (P >= 0 && A >= 0 && A < p.max_path && A < CP_MAX_ROWS) ? 1 : 0;
@@ -123,8 +125,8 @@ tv_status launch_compact(const CompactArgs& a) {
         return TV_ERR_CUDA;
     dim3 grid(a.Hkv, a.B, 2 * a.num_layers);
     if (grid.y > 65535 || grid.z > 65535) return TV_ERR_UNSUPPORTED;
-    kv_compact_kernel<<<grid, CP_THREADS, smem, a.stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    LaunchCfg lc(grid, dim3(CP_THREADS), smem, a.stream);
+    return cudaLaunchKernelEx(&lc.cfg, kv_compact_kernel, p) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
 }  // namespace tv

@@ -15,6 +15,8 @@ tree_mask_kernel(const int32_t* __restrict__ parents, int B, int N, uint64_t* __
     __shared__ int32_t spar[kMaskWarps][64];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * kMaskWarps + w;
+    pdl_launch_dependents();
+    pdl_wait();
     if (b >= B) return;
     const int32_t* par = parents + (int64_t)b * N;
     bool ok = true;
@@ -44,8 +46,11 @@ tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask,
                            int32_t* status, cudaStream_t stream) {
     if (B == 0) return TV_OK;
     dim3 grid((B + kMaskWarps - 1) / kMaskWarps);
-    tree_mask_kernel<<<grid, 32 * kMaskWarps, 0, stream>>>(parents, B, N, mask, depth, status);
-    return cudaGetLastError() == cudaSuccess ? TV_OK : TV_ERR_CUDA;
+    LaunchCfg lc(grid, dim3(32 * kMaskWarps), 0, stream);
+    return cudaLaunchKernelEx(&lc.cfg, tree_mask_kernel, parents, B, N, mask, depth, status) ==
+                   cudaSuccess
+               ? TV_OK
+               : TV_ERR_CUDA;
 }
 
 }  // namespace tv

@@ -25,6 +25,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Every kernel here is launched with programmatic stream serialisation, so it
+// may be scheduled while the previous kernel in the stream is still running.
+// pdl_launch_dependents lets the next kernel be scheduled as soon as all CTAs
+// of this grid have started; pdl_wait blocks until the previous grid has
+// completed and its memory operations are visible.  Each kernel calls pdl_wait
+// before its first global-memory access, so stream order is preserved.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

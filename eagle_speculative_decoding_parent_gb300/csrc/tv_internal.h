@@ -5,10 +5,53 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "treeverify.h"
 
 namespace tv {
+
+// Launch configuration used for every kernel: programmatic stream
+// serialisation (the kernel may be scheduled while the previous kernel in the
+// stream drains; each kernel waits with griddepcontrol.wait before touching
+// global memory) plus an optional cluster shape.  Setting TV_PDL=0 in the
+// environment launches with plain stream order instead.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("TV_PDL");
+        return !(e && strcmp(e, "0") == 0);
+    }();
+    return on;
+}
+
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, unsigned cluster = 0) {
+        memset(&cfg, 0, sizeof(cfg));
+        memset(attr, 0, sizeof(attr));
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        unsigned n = 0;
+        if (cluster > 0) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = cluster;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl_enabled()) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    }
+};
 
 // Multiprocessor count and opt-in shared memory of the current device (cached per device).
 int device_sm_count();
