@@ -80,11 +80,15 @@ struct Group {
     bool ok;
 };
 
-__device__ __forceinline__ Group decode_group(const Params& p, int gi, int rank, int cs) {
+// Group gi: sequence (in longest-first order when `order` is given), kv head,
+// row tile; this CTA's share of its key tiles.
+__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int gi, int rank,
+                                             int cs) {
     Group gr;
     gr.qt = gi % p.QT;
     gr.g = (gi / p.QT) % p.Hkv;
     gr.b = gi / (p.QT * p.Hkv);
+    if (order) gr.b = order[gr.b];
     gr.P = p.prefix_lens[gr.b];
     gr.L = gr.P + p.N;
     gr.ok = seq_ok_warp(p, gr.b, gr.P);
@@ -124,6 +128,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     uint64_t* xfree = xready + 1;
     int* gq = reinterpret_cast<int*>(xfree + 1);  // [GQ]
     int* flags = gq + GQ;                          // [0] abort
+    int* lpt = flags + 4;                          // [2][LPT_MAX] sequence lengths, order
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), cs = cluster_size();
@@ -147,6 +152,11 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     // every CTA of the cluster has initialised its barriers before any remote arrive
     cluster_barrier_all();
     pdl_wait();  // everything above touched only shared memory
+    const int* order = nullptr;
+    if (p.B <= LPT_MAX) {
+        lpt_order(p.prefix_lens, p.B, lpt, lpt + LPT_MAX);
+        order = lpt + LPT_MAX;
+    }
 
     if (warp == CONSUMER_WARPS) {
         // =========================== producer ===========================
@@ -174,12 +184,25 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             __syncwarp();
             if (lane == 0) remote_arrive(&gq_empty[slot], 0);
             if (gi >= p.groups) break;
-            const Group gr = decode_group(p, gi, rank, cs);
+            const Group gr = decode_group(p, order, gi, rank, cs);
             // block id of the page holding logical position tk (0 past the sequence end)
-            auto page_block = [&](int tk) -> int {
-                return (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+            // cache rows of the group's 16-key pages, 32 pages (8 tiles) per window:
+            // lane l holds page l of the current window as a row index, and the
+            // block id (loaded 8 tiles ahead) and row-in-block of the next window
+            constexpr int WIN_TILES = 32 / (KT / 16);
+            int nxt_blk = 0, nxt_off = 0;
+            auto load_window = [&](int w) {
+                const int tk = (gr.t_lo * (KT / 16) + w * 32 + lane) * 16;
+                nxt_blk = (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+                nxt_off = tk % p.bs;
             };
-            int blk_cur = (gr.t_lo < gr.t_hi && lane < KT / 16) ? page_block(gr.t_lo * KT + lane * 16) : 0;
+            auto row_of = [&]() -> int { return (nxt_blk * p.Hkv + gr.g) * p.bs + nxt_off; };
+            int win_y = 0;
+            if (gr.t_lo < gr.t_hi) {
+                load_window(0);
+                win_y = row_of();
+            }
+            if (gr.t_lo + WIN_TILES < gr.t_hi) load_window(1);
             for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
                 const int s = gt % STAGES;
                 const uint32_t ph = (gt / STAGES) & 1u;
@@ -202,21 +225,26 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                 uint64_t* bar = tail ? tail_bar : &full_bar[s];
                 uint8_t* kt = ring + s * LY::STAGE_BYTES;
                 uint8_t* vt = kt + LY::TILE_BYTES;
-                // one lane per 16-key page: lane 0 posts the byte count, then every
-                // page's lane issues its own copies with the block id it already holds
-                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-                __syncwarp();
-                if (lane < pages) {
-                    const int tk = t0 + lane * 16;
-                    const int y = (blk_cur * p.Hkv + gr.g) * p.bs + (tk % p.bs);
+                // the window holds every page's cache row; the warp walks the pages with
+                // that row broadcast and one elected lane issues the byte count and copies
+                mbar_arrive_expect_tx_elect(bar, bytes);
 #pragma unroll
-                    for (int hf = 0; hf < D / 64; ++hf) {
-                        tma_load_2d(kt + hf * (KT * 128) + lane * 2048, &kmap, bar, hf * 64, y, policy);
-                        tma_load_2d(vt + hf * (KT * 128) + lane * 2048, &vmap, bar, hf * 64, y, policy);
+                for (int j = 0; j < KT / 16; ++j) {
+                    const int y = __shfl_sync(0xffffffffu, win_y,
+                                              ((t - gr.t_lo) % WIN_TILES) * (KT / 16) + j);
+                    if (j < pages) {
+#pragma unroll
+                        for (int hf = 0; hf < D / 64; ++hf) {
+                            tma_load_2d_elect(kt + hf * (KT * 128) + j * 2048, &kmap, bar, hf * 64, y, policy);
+                            tma_load_2d_elect(vt + hf * (KT * 128) + j * 2048, &vmap, bar, hf * 64, y, policy);
+                        }
                     }
                 }
-                // block ids for the next tile, one page per lane, while this one is in flight
-                if (t + 1 < gr.t_hi && lane < KT / 16) blk_cur = page_block((t + 1) * KT + lane * 16);
+                if ((t - gr.t_lo) % WIN_TILES == WIN_TILES - 1 && t + 1 < gr.t_hi) {
+                    const int w = (t - gr.t_lo) / WIN_TILES + 1;   // window of tile t + 1
+                    win_y = row_of();
+                    if (gr.t_lo + (w + 1) * WIN_TILES < gr.t_hi) load_window(w + 1);
+                }
                 if (tail) {
                     // wait for the partial tile, zero the V rows past the sequence end
                     // (they may hold anything), then publish the stage
@@ -256,7 +284,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             __syncwarp();
             if (lane == 0) remote_arrive(&gq_empty[slot], 0);
             if (gi >= p.groups) break;
-            const Group gr = decode_group(p, gi, rank, cs);
+            const Group gr = decode_group(p, order, gi, rank, cs);
             if (rank == 0 && tid == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
             const int ntiles = gr.t_hi - gr.t_lo;
@@ -581,7 +609,8 @@ size_t smem_bytes() {
     constexpr int QROWS = WM * 16;
     return 1024 + Layout<D>::RING_BYTES + (size_t)(WK - 1) * QROWS * (D + 2) * 4 +
            (size_t)QROWS * Layout<D>::XO_STRIDE * 4 + (size_t)QROWS * MAX_CS * 4 +
-           (size_t)QROWS * 4 + (2 * STAGES + 1 + 2 * GQ + 2) * 8 + GQ * 4 + 16;
+           (size_t)QROWS * 4 + (2 * STAGES + 1 + 2 * GQ + 2) * 8 + GQ * 4 + 16 +
+           2 * LPT_MAX * 4;
 }
 
 // Clusters resident at once for cluster size cs (0 if the launch cannot fit).

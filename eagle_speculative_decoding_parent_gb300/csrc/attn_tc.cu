@@ -8,19 +8,23 @@
 // kv head for each), rows r = node * G + head, so one TMA box loads it.
 //
 // CTA roles (256 threads, one CTA per SM)
-//   warp 0   producer: Q tile (3-D TMA box), then 64-key K/V tiles (one 2-D
-//            box per 16-key page and 64-column half) through a 3-stage ring;
+//   warp 0   producer of Q (3-D TMA box per row tile) and K: 64-key tiles, one
+//            2-D box per 16-key page and 64-column half, into a 5-stage ring (4 when a cluster splits the group);
 //            in rank 0 also fetches group ids for the cluster.
-//   warp 1   MMA issuer (one thread): S = Q K^T into tensor memory (M=128,
-//            N=64, K=16 steps), O += P V (M=128, N=128, B operand N-major),
-//            completion signalled with tcgen05.commit.
-//   warp 2   allocates / frees 256 tensor-memory columns: S double buffer
-//            (2 x 64) and O (128).
+//   warp 2   producer of V into the same stages (each stage's full barrier
+//            waits for both producers); also allocates / frees 512 tensor-
+//            memory columns: S double buffer (2 x 64), O (128), P (2 x 32).
+//   warp 1   MMA issuer: S = Q K^T into tensor memory (M=128, N=64, K=16
+//            steps, both operands in shared memory), O += P V (M=128, N=128,
+//            P read from tensor memory, V N-major in shared memory);
+//            completion signalled with tcgen05.commit.  Every tcgen05 and TMA
+//            instruction is issued by an elect.sync-chosen lane of a converged
+//            warp.
 //   warps 4-7 softmax: thread i owns row i (tensor-memory lane i); reads S,
 //            applies scale and tree mask, keeps a running max that is only
 //            raised (and O rescaled in tensor memory) when it grows by more
-//            than 2^8, writes P (bf16) to shared memory for the PV product,
-//            and finally normalises O.
+//            than 2^8, writes P (bf16 pairs) to tensor memory for the PV
+//            product, and finally normalises O.
 #include <algorithm>
 
 #include "tv_device.cuh"
@@ -32,7 +36,8 @@ namespace tv {
 namespace {
 
 constexpr int KT = 64;        // keys per tile
-constexpr int STAGES = 4;
+constexpr int STAGES = 5;           // K/V ring depth when a CTA owns whole groups
+constexpr int STAGES_CLUSTER = 4;   // with a cluster split the fifth stage holds the merge rows
 constexpr int GQ = 4;
 constexpr int THREADS = 256;
 constexpr int SOFTMAX_WARP0 = 4;
@@ -50,16 +55,17 @@ constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr int TILE_BYTES = KT * D * 2;                 // 16 KB: one K or V tile
 constexpr int OFF_RING = 0;                            // STAGES x (K, V)
+constexpr int XO_BYTES = 128 * D * 2;                  // fp16 normalised O rows, 32 KB,
+constexpr int OFF_XO = OFF_RING + STAGES_CLUSTER * 2 * TILE_BYTES;  // in the fifth stage
 constexpr int OFF_Q = OFF_RING + STAGES * 2 * TILE_BYTES;
 constexpr int Q_BYTES = 128 * D * 2;                   // 32 KB
-constexpr int OFF_XO = OFF_Q + Q_BYTES;                // fp16 normalised O rows, 32 KB
-constexpr int XO_BYTES = 128 * D * 2;
-constexpr int OFF_XML = OFF_XO + XO_BYTES;             // (max, sum) per row
+constexpr int OFF_XML = OFF_Q + Q_BYTES;               // (max, sum) per row
 constexpr int OFF_WTS = OFF_XML + 128 * 8;             // merge weights [128][MAX_CS]
 constexpr int OFF_BARS = OFF_WTS + 128 * MAX_CS * 4;
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 1 + 2 * GQ + 2;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;       // + alignment slack
+constexpr int OFF_LPT = OFF_MISC + 64;                 // sequence order: lens, order
+constexpr int SMEM_BYTES = OFF_LPT + 2 * LPT_MAX * 4 + 1024;  // + alignment slack
 
 struct Params {
     const int32_t* table;
@@ -90,11 +96,15 @@ __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ Group decode_group(const Params& p, int gi, int rank, int cs) {
+// Group gi: sequence (in longest-first order when `order` is given), kv head,
+// row tile; this CTA's share of its key tiles.
+__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int gi, int rank,
+                                             int cs) {
     Group gr;
     gr.qt = gi % p.QT;
     gr.g = (gi / p.QT) % p.Hkv;
     gr.b = gi / (p.QT * p.Hkv);
+    if (order) gr.b = order[gr.b];
     gr.P = p.prefix_lens[gr.b];
     gr.L = gr.P + p.N;
     gr.ok = seq_ok_warp(p, gr.b, gr.P);
@@ -134,11 +144,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), cs = cluster_size();
     const uint32_t sbase = smem_u32(smem);
+    const uint32_t nst = (cs == 1) ? STAGES : STAGES_CLUSTER;  // K/V ring depth
     pdl_launch_dependents();
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&kfull[s], 1);
+            mbar_init(&kfull[s], 2);              // K producer + V producer
             mbar_init(&kempty[s], 1);
         }
         mbar_init(qfull, 1);
@@ -154,7 +165,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_init(tailb, 1);
         for (int s = 0; s < GQ; ++s) {
             mbar_init(&gq_full[s], 1);
-            mbar_init(&gq_empty[s], cs * 6);
+            mbar_init(&gq_empty[s], cs * 7);      // 2 producers, MMA, 4 softmax warps
         }
         mbar_init(xready, cs * 4);
         mbar_init(xfree, cs * 4);
@@ -170,6 +181,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_after();
     pdl_wait();  // everything above touched only shared memory and TMEM
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_base_slot);
+    const int* order = nullptr;
+    if (p.B <= LPT_MAX) {
+        int* lpt = reinterpret_cast<int*>(smem + OFF_LPT);
+        lpt_order(p.prefix_lens, p.B, lpt, lpt + LPT_MAX);
+        order = lpt + LPT_MAX;
+    }
 
     // group id k of this CTA (all roles walk the same sequence)
     auto next_group = [&](uint32_t k, bool fetcher) -> int {
@@ -189,45 +206,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         return gi;
     };
 
-    if (warp == 0) {
-        // =========================== producer ===========================
+    if (warp == 0 || warp == 2) {
+        // ============ producers: warp 0 loads Q and K, warp 2 loads V ============
+        // (two warps on different schedulers: each issues half of a tile's copies)
+        const bool kprod = (warp == 0);
+        const CUtensorMap* map = kprod ? &kmap : &vmap;
         if (lane == 0) {
-            tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
+            if (kprod) tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(map);
         }
         const uint64_t policy = (p.QT == 1) ? l2_policy_evict_first() : l2_policy_evict_normal();
         uint32_t gt = 0, qi = 0, tail_phase = 0;
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
-            const int gi = next_group(k, rank == 0);
+            const int gi = next_group(k, kprod && rank == 0);
             if (gi >= p.groups) break;
-            const Group gr = decode_group(p, gi, rank, cs);
+            const Group gr = decode_group(p, order, gi, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
-            // Q tile: npt nodes x G heads x 128 columns
-            if (lane == 0) {
-                bool ok = mbar_wait(qempty, (qi & 1u) ^ 1u);
-                if (!ok) {
-                    flags[0] = 1;
-                    p.status[gr.b] = TV_ERR_TIMEOUT;
+            if (kprod) {
+                // Q tile: npt nodes x G heads x 128 columns
+                if (lane == 0) {
+                    bool ok = mbar_wait(qempty, (qi & 1u) ^ 1u);
+                    if (!ok) {
+                        flags[0] = 1;
+                        p.status[gr.b] = TV_ERR_TIMEOUT;
+                    }
+                    const uint32_t qbytes = 2u * 64u * (uint32_t)(p.G * p.npt) * 2u;
+                    mbar_arrive_expect_tx(qfull, qbytes);
+                    const int node0 = gr.b * p.N + gr.qt * p.npt;
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(smem + OFF_Q + hf * (128 * 128), &qmap, qfull, hf * 64,
+                                    gr.g * p.G, node0);
                 }
-                const uint32_t qbytes = 2u * 64u * (uint32_t)(p.G * p.npt) * 2u;
-                mbar_arrive_expect_tx(qfull, qbytes);
-                const int node0 = gr.b * p.N + gr.qt * p.npt;
-                for (int hf = 0; hf < 2; ++hf)
-                    tma_load_3d(smem + OFF_Q + hf * (128 * 128), &qmap, qfull, hf * 64, gr.g * p.G,
-                                node0);
+                ++qi;
             }
-            ++qi;
-            // block id of the page holding logical position tk (0 past the sequence end)
-            auto page_block = [&](int tk) -> int {
-                return (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+            // cache rows of the group's 16-key pages, 32 pages (8 tiles) per window:
+            // lane l holds page l of the current window as a row index, and the
+            // block id (loaded 8 tiles ahead) and row-in-block of the next window
+            constexpr int WIN_TILES = 32 / (KT / 16);
+            int nxt_blk = 0, nxt_off = 0;
+            auto load_window = [&](int w) {
+                const int tk = (gr.t_lo * (KT / 16) + w * 32 + lane) * 16;
+                nxt_blk = (tk < gr.L) ? __ldg(p.table + (int64_t)gr.b * p.max_blocks + tk / p.bs) : 0;
+                nxt_off = tk % p.bs;
             };
-            int blk_cur = (gr.t_lo < gr.t_hi && lane < KT / 16) ? page_block(gr.t_lo * KT + lane * 16) : 0;
+            auto row_of = [&]() -> int { return (nxt_blk * p.Hkv + gr.g) * p.bs + nxt_off; };
+            int win_y = 0;
+            if (gr.t_lo < gr.t_hi) {
+                load_window(0);
+                win_y = row_of();
+            }
+            if (gr.t_lo + WIN_TILES < gr.t_hi) load_window(1);
             for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
-                const int s = gt % STAGES;
-                const uint32_t ph = (gt / STAGES) & 1u;
+                const int s = gt % nst;
+                const uint32_t ph = (gt / nst) & 1u;
                 bool freed = !*(volatile int*)&flags[0];
                 if (lane == 0 && freed) freed = mbar_wait(&kempty[s], ph ^ 1u);
                 freed = __shfl_sync(0xffffffffu, freed, 0);
@@ -242,27 +275,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const int t0 = t * KT;
                 const int nv = min(KT, gr.L - t0);
                 const int pages = (nv + 15) >> 4;
-                const uint32_t bytes = (uint32_t)pages * 16u * D * 2u * 2u;
-                const bool tail = nv < KT;
-                uint64_t* bar = tail ? tailb : &kfull[s];
-                uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
-                uint8_t* vt = kt + TILE_BYTES;
-                // one lane per 16-key page: lane 0 posts the byte count, then every
-                // page's lane issues its own copies with the block id it already holds
-                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-                __syncwarp();
-                if (lane < pages) {
-                    const int tk = t0 + lane * 16;
-                    const int y = (blk_cur * p.Hkv + gr.g) * p.bs + (tk % p.bs);
+                const uint32_t bytes = (uint32_t)pages * 16u * D * 2u;
+                // a partial V tile lands on its own barrier: rows past the end are
+                // zeroed before the stage is published
+                const bool vtail = !kprod && nv < KT;
+                uint64_t* bar = vtail ? tailb : &kfull[s];
+                uint8_t* dst = smem + OFF_RING + s * 2 * TILE_BYTES + (kprod ? 0 : TILE_BYTES);
+                // the window holds every page's cache row; the warp walks the pages with
+                // that row broadcast and one elected lane issues the byte count and copies
+                mbar_arrive_expect_tx_elect(bar, bytes);
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tma_load_2d(kt + hf * (KT * 128) + lane * 2048, &kmap, bar, hf * 64, y, policy);
-                        tma_load_2d(vt + hf * (KT * 128) + lane * 2048, &vmap, bar, hf * 64, y, policy);
+                for (int j = 0; j < KT / 16; ++j) {
+                    const int y = __shfl_sync(0xffffffffu, win_y,
+                                              ((t - gr.t_lo) % WIN_TILES) * (KT / 16) + j);
+                    if (j < pages) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_2d_elect(dst + hf * (KT * 128) + j * 2048, map, bar, hf * 64, y,
+                                              policy);
                     }
                 }
-                // block ids for the next tile, one page per lane, while this one is in flight
-                if (t + 1 < gr.t_hi && lane < KT / 16) blk_cur = page_block((t + 1) * KT + lane * 16);
-                if (tail) {
+                if ((t - gr.t_lo) % WIN_TILES == WIN_TILES - 1 && t + 1 < gr.t_hi) {
+                    const int w = (t - gr.t_lo) / WIN_TILES + 1;   // window of tile t + 1
+                    win_y = row_of();
+                    if (gr.t_lo + (w + 1) * WIN_TILES < gr.t_hi) load_window(w + 1);
+                }
+                if (vtail) {
                     const bool landed = __all_sync(0xffffffffu, mbar_wait(tailb, tail_phase));
                     tail_phase ^= 1u;
                     if (!landed) {
@@ -279,7 +317,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const int hf = e / (zrows * 8);
                         const int r = nv + (e / 8) % zrows;
                         const int ch = e % 8;
-                        *reinterpret_cast<uint4*>(vt + hf * (KT * 128) + r * 128 + ch * 16) =
+                        *reinterpret_cast<uint4*>(dst + hf * (KT * 128) + r * 128 + ch * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();  // the tensor core reads V through the async proxy
@@ -300,18 +338,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (!wait_all(&pfull[pb], (t >> 1) & 1u)) return false;
             if (first && og > 0 && !wait_all(ofree, (og - 1) & 1u)) return false;
             tc_fence_after();
-            if (lane == 0) {
-                const int s = t % STAGES;
+            {
+                const int s = t % nst;
                 const uint32_t pa = tmem + TMEM_P + pb * (KT / 2);
                 const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
                     const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
-                    tc_mma_bf16_ts(tO, pa + kk * 8, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
+                    tc_mma_bf16_ts_elect(tO, pa + kk * 8, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
                 }
-                tc_commit(&kempty[s]);
-                tc_commit(&pfree[pb]);
-                tc_commit(pvdone);
+                tc_commit_elect(&kempty[s]);
+                tc_commit_elect(&pfree[pb]);
+                tc_commit_elect(pvdone);
             }
             __syncwarp();
             return true;
@@ -320,31 +358,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (uint32_t k = 0; alive; ++k) {
             const int gi = next_group(k, false);
             if (gi >= p.groups) break;
-            const Group gr = decode_group(p, gi, rank, cs);
+            const Group gr = decode_group(p, order, gi, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
             if (!wait_all(qfull, qi & 1u)) { alive = false; break; }
             ++qi;
             const uint32_t first_tile = gt;
             for (int j = 0; j < n; ++j, ++gt) {
-                const int s = gt % STAGES, sb = gt & 1;
-                if (!wait_all(&kfull[s], (gt / STAGES) & 1u) ||
+                const int s = gt % nst, sb = gt & 1;
+                if (!wait_all(&kfull[s], (gt / nst) & 1u) ||
                     !wait_all(&sfree[sb], ((gt >> 1) & 1u) ^ 1u)) {
                     alive = false;
                     break;
                 }
                 tc_fence_after();
-                if (lane == 0) {
+                {
                     const uint32_t qa = sbase + OFF_Q;
                     const uint32_t ka = sbase + OFF_RING + s * 2 * TILE_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * (KT * 128) + (kk & 3) * 32, 16, 1024);
-                        tc_mma_bf16(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+                        tc_mma_bf16_elect(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(&sfull[sb]);
-                    if (j == n - 1) tc_commit(qempty);
+                    tc_commit_elect(&sfull[sb]);
+                    if (j == n - 1) tc_commit_elect(qempty);
                 }
                 __syncwarp();
                 if (j > 0 && !do_pv(gt - 1, gt - 1 == first_tile)) {
@@ -380,7 +418,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (uint32_t k = 0;; ++k) {
             const int gi = next_group(k, false);
             if (gi >= p.groups) break;
-            const Group gr = decode_group(p, gi, rank, cs);
+            const Group gr = decode_group(p, order, gi, rank, cs);
             if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
             const int n = gr.t_hi - gr.t_lo;
@@ -413,7 +451,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sfree[sb]);
                 const int t0 = (gr.t_lo + j) * KT;
-                float tmax = -INFINITY;
                 if (t0 + KT > gr.P) {
 #pragma unroll
                     for (int c = 0; c < KT; ++c) {
@@ -421,12 +458,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         const bool vis = (t < gr.P) ||
                                          (t < gr.L && ((mk >> (t - gr.P)) & 1ull));
                         sv[c] = vis ? sv[c] : -INFINITY;
-                        tmax = fmaxf(tmax, sv[c]);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < KT; ++c) tmax = fmaxf(tmax, sv[c]);
                 }
+                // row maximum as a tree of eight independent chains
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[i + 8]);
+#pragma unroll
+                for (int c = 16; c < KT; c += 8)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], sv[c + i]);
+                float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                 tmax *= p.scale_log2;  // scores stay unscaled; the scale is folded into the exponent
                 const float m_new = fmaxf(m_used, tmax);
                 const bool need = (m_used == -INFINITY) ? (m_new > -INFINITY)
@@ -457,15 +500,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
                 const float csc = p.scale_log2;
                 uint32_t pk[KT / 2];
-                float rs = 0.f;
+                float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < KT; c += 2) {
                     const float a = ex2_approx(fmaf(sv[c], csc, nbase));
                     const float b2 = ex2_approx(fmaf(sv[c + 1], csc, nbase));
-                    rs += a + b2;
+                    rs[(c >> 1) & 3] += a + b2;
                     pk[c / 2] = pack_bf16x2(a, b2);
                 }
-                l += rs;
+                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
                 // P row -> tensor memory (this thread's lane) once its buffer is free
                 const int pb = gt & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&pfree[pb], ((gt >> 1) & 1u) ^ 1u))) {

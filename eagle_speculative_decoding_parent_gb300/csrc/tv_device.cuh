@@ -37,6 +37,29 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ------------------------------------------------------------- work order
+// Batches up to this size are processed longest sequence first.
+constexpr int LPT_MAX = 256;
+
+// Longest-first order of a batch: order[r] is the r-th longest sequence by
+// prefix length (ties by index), so dynamically scheduled work starts with the
+// longest groups and the short ones fill in at the end.  Called by every thread
+// of the CTA; lens[B] and order[B] live in shared memory, B <= LPT_MAX.
+__device__ __forceinline__ void lpt_order(const int32_t* prefix_lens, int B, int* lens, int* order) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) lens[b] = prefix_lens[b];
+    __syncthreads();
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        const int lb = lens[b];
+        int r = 0;
+        for (int j = 0; j < B; ++j) {
+            const int lj = lens[j];
+            r += (lj > lb) || (lj == lb && j < b);
+        }
+        order[r] = b;
+    }
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -94,6 +117,26 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+// Warp-collective forms (every lane of a converged warp calls them with the
+// same arguments): one lane chosen by elect.sync performs the operation.  The
+// warp stays converged, so the operands can stay in uniform registers; issuing
+// from an `if (lane == 0)` branch instead costs tens of cycles per instruction.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_elect(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                  int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
