@@ -80,18 +80,27 @@ struct Group {
     bool ok;
 };
 
-// Group gi: sequence (in longest-first order when `order` is given), kv head,
-// row tile; this CTA's share of its key tiles.
-__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int gi, int rank,
+// Group ids travel with a validity bit: the fetching warp checks the group's
+// sequence once (seq_ok_warp) and marks a bad one with GROUP_BAD.
+constexpr int GROUP_BAD = 1 << 30;
+
+__device__ __forceinline__ int group_seq(const Params& p, const int* order, int gi) {
+    const int r = gi / (p.QT * p.Hkv);
+    return order ? order[r] : r;
+}
+
+// Fetched word -> group: sequence (in longest-first order when `order` is
+// given), kv head, row tile; this CTA's share of its key tiles.
+__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int word, int rank,
                                              int cs) {
     Group gr;
+    const int gi = word & (GROUP_BAD - 1);
     gr.qt = gi % p.QT;
     gr.g = (gi / p.QT) % p.Hkv;
-    gr.b = gi / (p.QT * p.Hkv);
-    if (order) gr.b = order[gr.b];
+    gr.b = group_seq(p, order, gi);
     gr.P = p.prefix_lens[gr.b];
     gr.L = gr.P + p.N;
-    gr.ok = seq_ok_warp(p, gr.b, gr.P);
+    gr.ok = (word & GROUP_BAD) == 0;
     const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
     gr.t_lo = (int)((int64_t)T * rank / cs);
     gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
@@ -170,12 +179,22 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
         for (uint32_t k = 0; alive; ++k) {
             const int slot = k % GQ;
             // rank 0 fetches the next group id and hands it to the whole cluster
-            if (rank == 0 && lane == 0) {
-                bool ok = mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u);
-                const int gi = ok ? atomicAdd(&p.sched[0], 1) : p.groups;
-                for (uint32_t r = 0; r < cs; ++r) {
-                    remote_st_u32(&gq[slot], r, gi);
-                    remote_arrive(&gq_full[slot], r);
+            // (the producer warp also validates the group's sequence, once)
+            if (rank == 0) {
+                int gi = p.groups;
+                if (lane == 0 && mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u))
+                    gi = atomicAdd(&p.sched[0], 1);
+                gi = __shfl_sync(0xffffffffu, gi, 0);
+                int word = gi;
+                if (gi < p.groups) {
+                    const int b = group_seq(p, order, gi);
+                    if (!seq_ok_warp(p, b, p.prefix_lens[b])) word |= GROUP_BAD;
+                }
+                if (lane == 0) {
+                    for (uint32_t r = 0; r < cs; ++r) {
+                        remote_st_u32(&gq[slot], r, word);
+                        remote_arrive(&gq_full[slot], r);
+                    }
                 }
             }
             // every lane acquires the slot written by rank 0 before reading it
@@ -183,7 +202,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int gi = got ? *(volatile int*)&gq[slot] : p.groups;
             __syncwarp();
             if (lane == 0) remote_arrive(&gq_empty[slot], 0);
-            if (gi >= p.groups) break;
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group(p, order, gi, rank, cs);
             // block id of the page holding logical position tk (0 past the sequence end)
             // cache rows of the group's 16-key pages, 32 pages (8 tiles) per window:
@@ -283,7 +302,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             const int gi = got ? *(volatile int*)&gq[slot] : p.groups;
             __syncwarp();
             if (lane == 0) remote_arrive(&gq_empty[slot], 0);
-            if (gi >= p.groups) break;
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group(p, order, gi, rank, cs);
             if (rank == 0 && tid == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;

@@ -55,8 +55,9 @@ constexpr uint32_t IDESC_PV = idesc_bf16(128, D, true);
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr int TILE_BYTES = KT * D * 2;                 // 16 KB: one K or V tile
 constexpr int OFF_RING = 0;                            // STAGES x (K, V)
-constexpr int XO_BYTES = 128 * D * 2;                  // fp16 normalised O rows, 32 KB,
-constexpr int OFF_XO = OFF_RING + STAGES_CLUSTER * 2 * TILE_BYTES;  // in the fifth stage
+// fp16 normalised O rows for the cluster merge (128 x 128 x 2 = one stage) in the fifth stage
+constexpr int OFF_XO = OFF_RING + STAGES_CLUSTER * 2 * TILE_BYTES;
+static_assert(128 * D * 2 <= 2 * TILE_BYTES, "merge rows fit in one ring stage");
 constexpr int OFF_Q = OFF_RING + STAGES * 2 * TILE_BYTES;
 constexpr int Q_BYTES = 128 * D * 2;                   // 32 KB
 constexpr int OFF_XML = OFF_Q + Q_BYTES;               // (max, sum) per row
@@ -96,18 +97,27 @@ __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     return __all_sync(0xffffffffu, ok);
 }
 
-// Group gi: sequence (in longest-first order when `order` is given), kv head,
-// row tile; this CTA's share of its key tiles.
-__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int gi, int rank,
+// Group ids travel with a validity bit: the fetching warp checks the group's
+// sequence once (seq_ok_warp) and marks a bad one with GROUP_BAD.
+constexpr int GROUP_BAD = 1 << 30;
+
+__device__ __forceinline__ int group_seq(const Params& p, const int* order, int gi) {
+    const int r = gi / (p.QT * p.Hkv);
+    return order ? order[r] : r;
+}
+
+// Fetched word -> group: sequence (in longest-first order when `order` is
+// given), kv head, row tile; this CTA's share of its key tiles.
+__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int word, int rank,
                                              int cs) {
     Group gr;
+    const int gi = word & (GROUP_BAD - 1);
     gr.qt = gi % p.QT;
     gr.g = (gi / p.QT) % p.Hkv;
-    gr.b = gi / (p.QT * p.Hkv);
-    if (order) gr.b = order[gr.b];
+    gr.b = group_seq(p, order, gi);
     gr.P = p.prefix_lens[gr.b];
     gr.L = gr.P + p.N;
-    gr.ok = seq_ok_warp(p, gr.b, gr.P);
+    gr.ok = (word & GROUP_BAD) == 0;
     const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
     gr.t_lo = (int)((int64_t)T * rank / cs);
     gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
@@ -189,14 +199,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
 
     // group id k of this CTA (all roles walk the same sequence)
+    // (the fetcher is a whole warp: it also validates the group's sequence)
     auto next_group = [&](uint32_t k, bool fetcher) -> int {
         const int slot = k % GQ;
-        if (fetcher && lane == 0) {
-            const bool ok = mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u);
-            const int gi = ok ? atomicAdd(&p.sched[0], 1) : p.groups;
-            for (uint32_t r = 0; r < cs; ++r) {
-                remote_st_u32(&gq[slot], r, gi);
-                remote_arrive(&gq_full[slot], r);
+        if (fetcher) {
+            int gi = p.groups;
+            if (lane == 0 && mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u))
+                gi = atomicAdd(&p.sched[0], 1);
+            gi = __shfl_sync(0xffffffffu, gi, 0);
+            int word = gi;
+            if (gi < p.groups) {
+                const int b = group_seq(p, order, gi);
+                if (!seq_ok_warp(p, b, p.prefix_lens[b])) word |= GROUP_BAD;
+            }
+            if (lane == 0) {
+                for (uint32_t r = 0; r < cs; ++r) {
+                    remote_st_u32(&gq[slot], r, word);
+                    remote_arrive(&gq_full[slot], r);
+                }
             }
         }
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&gq_full[slot], (k / GQ) & 1u));
@@ -220,7 +240,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
             const int gi = next_group(k, kprod && rank == 0);
-            if (gi >= p.groups) break;
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group(p, order, gi, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
@@ -357,7 +377,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
             const int gi = next_group(k, false);
-            if (gi >= p.groups) break;
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group(p, order, gi, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
@@ -417,7 +437,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         };
         for (uint32_t k = 0;; ++k) {
             const int gi = next_group(k, false);
-            if (gi >= p.groups) break;
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group(p, order, gi, rank, cs);
             if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
