@@ -14,12 +14,14 @@
 //   warp 2   producer of V into the same stages (each stage's full barrier
 //            waits for both producers); also allocates / frees 512 tensor-
 //            memory columns: S double buffer (2 x 64), O (128), P (2 x 32).
-//   warp 1   MMA issuer: S = Q K^T into tensor memory (M=128, N=64, K=16
-//            steps, both operands in shared memory), O += P V (M=128, N=128,
-//            P read from tensor memory, V N-major in shared memory);
-//            completion signalled with tcgen05.commit.  Every tcgen05 and TMA
-//            instruction is issued by an elect.sync-chosen lane of a converged
-//            warp.
+//   warp 1   S issuer: S = Q K^T into tensor memory (M=128, N=64, K=16 steps,
+//            both operands in shared memory), double-buffered S.
+//   warp 3   PV issuer: O += P V (M=128, N=128, P read from tensor memory, V
+//            N-major in shared memory), in tile order; releases the K/V stage.
+//            Completion is signalled with tcgen05.commit (it covers only the
+//            issuing thread's products, so each issuer commits its own).  Every
+//            tcgen05 and TMA instruction is issued by an elect.sync-chosen lane
+//            of a converged warp.
 //   warps 4-7 softmax: thread i owns row i (tensor-memory lane i); reads S,
 //            applies scale and tree mask, keeps a running max that is only
 //            raised (and O rescaled in tensor memory) when it grows by more
@@ -175,7 +177,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_init(tailb, 1);
         for (int s = 0; s < GQ; ++s) {
             mbar_init(&gq_full[s], 1);
-            mbar_init(&gq_empty[s], cs * 7);      // 2 producers, MMA, 4 softmax warps
+            mbar_init(&gq_empty[s], cs * 8);      // 2 producers, 2 MMA issuers, 4 softmax warps
         }
         mbar_init(xready, cs * 4);
         mbar_init(xfree, cs * 4);
@@ -224,6 +226,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         __syncwarp();
         if (lane == 0) remote_arrive(&gq_empty[slot], 0);
         return gi;
+    };
+
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity));
     };
 
     if (warp == 0 || warp == 2) {
@@ -347,33 +353,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
         }
     } else if (warp == 1) {
-        // =========================== MMA issuer ===========================
-        uint32_t gt = 0, qi = 0, og = 0;
-        const uint32_t tS = tmem, tO = tmem + TMEM_O;
-        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-            return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-        };
-        auto do_pv = [&](uint32_t t, bool first) -> bool {
-            const int pb = t & 1;
-            if (!wait_all(&pfull[pb], (t >> 1) & 1u)) return false;
-            if (first && og > 0 && !wait_all(ofree, (og - 1) & 1u)) return false;
-            tc_fence_after();
-            {
-                const int s = t % nst;
-                const uint32_t pa = tmem + TMEM_P + pb * (KT / 2);
-                const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < KT / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
-                    tc_mma_bf16_ts_elect(tO, pa + kk * 8, bd, IDESC_PV, (first && kk == 0) ? 0u : 1u);
-                }
-                tc_commit_elect(&kempty[s]);
-                tc_commit_elect(&pfree[pb]);
-                tc_commit_elect(pvdone);
-            }
-            __syncwarp();
-            return true;
-        };
+        // ===================== S issuer: S = Q K^T per tile =====================
+        uint32_t gt = 0, qi = 0;
+        const uint32_t tS = tmem;
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
             const int gi = next_group(k, false);
@@ -383,7 +365,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (n == 0) continue;
             if (!wait_all(qfull, qi & 1u)) { alive = false; break; }
             ++qi;
-            const uint32_t first_tile = gt;
             for (int j = 0; j < n; ++j, ++gt) {
                 const int s = gt % nst, sb = gt & 1;
                 if (!wait_all(&kfull[s], (gt / nst) & 1u) ||
@@ -392,26 +373,53 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     break;
                 }
                 tc_fence_after();
-                {
-                    const uint32_t qa = sbase + OFF_Q;
-                    const uint32_t ka = sbase + OFF_RING + s * 2 * TILE_BYTES;
+                const uint32_t qa = sbase + OFF_Q;
+                const uint32_t ka = sbase + OFF_RING + s * 2 * TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * (KT * 128) + (kk & 3) * 32, 16, 1024);
-                        tc_mma_bf16_elect(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
-                    }
-                    tc_commit_elect(&sfull[sb]);
-                    if (j == n - 1) tc_commit_elect(qempty);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * (KT * 128) + (kk & 3) * 32, 16, 1024);
+                    tc_mma_bf16_elect(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
+                tc_commit_elect(&sfull[sb]);
+                if (j == n - 1) tc_commit_elect(qempty);
                 __syncwarp();
-                if (j > 0 && !do_pv(gt - 1, gt - 1 == first_tile)) {
+            }
+        }
+        if (!alive && lane == 0) flags[0] = 1;
+    } else if (warp == 3) {
+        // ============ PV issuer: O += P V per tile, in tile order ============
+        // (its own warp, so PV products never queue behind a wait for K data)
+        uint32_t gt = 0, og = 0;
+        const uint32_t tO = tmem + TMEM_O;
+        bool alive = true;
+        for (uint32_t k = 0; alive; ++k) {
+            const int gi = next_group(k, false);
+            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
+            const Group gr = decode_group(p, order, gi, rank, cs);
+            const int n = gr.t_hi - gr.t_lo;
+            if (n == 0) continue;
+            for (int j = 0; j < n; ++j, ++gt) {
+                const int pb = gt & 1, s = gt % nst;
+                if (!wait_all(&pfull[pb], (gt >> 1) & 1u) ||
+                    (j == 0 && og > 0 && !wait_all(ofree, (og - 1) & 1u))) {
                     alive = false;
                     break;
                 }
+                tc_fence_after();
+                const uint32_t pa = tmem + TMEM_P + pb * (KT / 2);
+                const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < KT / 16; ++kk) {
+                    const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
+                    tc_mma_bf16_ts_elect(tO, pa + kk * 8, bd, IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
+                }
+                tc_commit_elect(&kempty[s]);
+                tc_commit_elect(&pfree[pb]);
+                tc_commit_elect(pvdone);
+                __syncwarp();
             }
             if (!alive) break;
-            if (!do_pv(gt - 1, gt - 1 == first_tile)) break;
             ++og;
         }
         if (!alive && lane == 0) flags[0] = 1;
@@ -677,7 +685,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (cs > 1 && merges > 0) mbar_wait_cluster(xfree, (merges - 1) & 1u);
         __syncwarp();
     }
-    // warps 2-3 (and every role once done) meet here
+    // every role meets here once done
     tc_fence_before();
     cluster_barrier_all();
     tc_fence_after();
