@@ -8,12 +8,14 @@
 // kv head for each), rows r = node * G + head, so one TMA box loads it.
 //
 // CTA roles (256 threads, one CTA per SM)
-//   warp 0   producer of Q (3-D TMA box per row tile) and K: 64-key tiles, one
-//            2-D box per 16-key page and 64-column half, into a 5-stage ring (4 when a cluster splits the group);
-//            in rank 0 also fetches group ids for the cluster.
-//   warp 2   producer of V into the same stages (each stage's full barrier
-//            waits for both producers); also allocates / frees 512 tensor-
-//            memory columns: S double buffer (2 x 64), O (128), P (2 x 32).
+//   warp 0   producer of Q (3-D TMA box per row tile) and of pages 0-1 of
+//            each 64-key K/V tile; warp 2 loads pages 2-3.  A 16-key page is
+//            two K boxes (one per 64-column half) and one V box holding both
+//            halves; the ring has 5 stages (4 when a cluster splits the group).
+//            Warp 0 of rank 0 also fetches group ids for the cluster and
+//            validates each group's block table; warp 2 also allocates / frees
+//            512 tensor-memory columns: S double buffer (2 x 64), O (128), P
+//            (2 x 32).
 //   warp 1   S issuer: S = Q K^T into tensor memory (M=128, N=64, K=16 steps,
 //            both operands in shared memory), double-buffered S.
 //   warp 3   PV issuer: O += P V (M=128, N=128, P read from tensor memory, V
@@ -161,7 +163,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&kfull[s], 2);              // K producer + V producer
+            mbar_init(&kfull[s], 2);              // both producers
             mbar_init(&kempty[s], 1);
         }
         mbar_init(qfull, 1);
@@ -175,7 +177,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_init(&pvdone[0], 1);
         mbar_init(&pvdone[1], 1);
         mbar_init(ofree, 4);
-        mbar_init(tailb, 1);
+        mbar_init(tailb, 2);
         for (int s = 0; s < GQ; ++s) {
             mbar_init(&gq_full[s], 1);
             mbar_init(&gq_empty[s], cs * 8);      // 2 producers, 2 MMA issuers, 4 softmax warps
@@ -234,13 +236,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     };
 
     if (warp == 0 || warp == 2) {
-        // ============ producers: warp 0 loads Q and K, warp 2 loads V ============
-        // (two warps on different schedulers: each issues half of a tile's copies)
+        // ==== producers: warp 0 loads Q and pages 0-1 of each tile, warp 2 pages 2-3 ====
+        // (two warps on different schedulers: each issues half of a tile's copies;
+        // a page is two K boxes, one per 64-column half, and one V box)
         const bool kprod = (warp == 0);
-        const CUtensorMap* map = kprod ? &kmap : &vmap;
+        const int pg0 = kprod ? 0 : KT / 32;
         if (lane == 0) {
             if (kprod) tma_prefetch_desc(&qmap);
-            tma_prefetch_desc(map);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
         }
         const uint64_t policy = (p.QT == 1) ? l2_policy_evict_first() : l2_policy_evict_normal();
         uint32_t gt = 0, qi = 0, tail_phase = 0;
@@ -302,24 +306,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const int t0 = t * KT;
                 const int nv = min(KT, gr.L - t0);
                 const int pages = (nv + 15) >> 4;
-                const uint32_t bytes = (uint32_t)pages * 16u * D * 2u;
-                // a partial V tile lands on its own barrier: rows past the end are
-                // zeroed before the stage is published
-                const bool vtail = !kprod && nv < KT;
-                uint64_t* bar = vtail ? tailb : &kfull[s];
-                uint8_t* dst = smem + OFF_RING + s * 2 * TILE_BYTES + (kprod ? 0 : TILE_BYTES);
-                // the window holds every page's cache row; the warp walks the pages with
+                const int mine = max(0, min(KT / 32, pages - pg0));  // this warp's pages
+                const uint32_t bytes = (uint32_t)mine * 16u * D * 2u * 2u;
+                // a partial tile lands on its own barrier: V rows past the end are
+                // zeroed by warp 0 before the stage is published
+                const bool tail = nv < KT;
+                uint64_t* bar = tail ? tailb : &kfull[s];
+                uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
+                uint8_t* vt = kt + TILE_BYTES;
+                // the window holds every page's cache row; the warp walks its pages with
                 // that row broadcast and one elected lane issues the byte count and copies
                 mbar_arrive_expect_tx_elect(bar, bytes);
 #pragma unroll
-                for (int j = 0; j < KT / 16; ++j) {
+                for (int jj = 0; jj < KT / 32; ++jj) {
+                    const int j = pg0 + jj;
                     const int y = __shfl_sync(0xffffffffu, win_y,
                                               ((t - gr.t_lo) % WIN_TILES) * (KT / 16) + j);
                     if (j < pages) {
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf)
-                            tma_load_2d_elect(dst + hf * (KT * 128) + j * 2048, map, bar, hf * 64, y,
-                                              policy);
+                        tma_load_2d_elect(kt + j * 2048, &kmap, bar, 0, y, policy);
+                        tma_load_2d_elect(kt + KT * 128 + j * 2048, &kmap, bar, 64, y, policy);
+                        tma_load_3d_elect(vt + j * 4096, &vmap, bar, 0, y, 0, policy);
                     }
                 }
                 if ((t - gr.t_lo) % WIN_TILES == WIN_TILES - 1 && t + 1 < gr.t_hi) {
@@ -327,7 +333,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     win_y = row_of();
                     if (gr.t_lo + (w + 1) * WIN_TILES < gr.t_hi) load_window(w + 1);
                 }
-                if (vtail) {
+                if (tail && !kprod) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kfull[s]);
+                } else if (tail) {
                     const bool landed = __all_sync(0xffffffffu, mbar_wait(tailb, tail_phase));
                     tail_phase ^= 1u;
                     if (!landed) {
@@ -338,14 +347,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                         alive = false;
                         break;
                     }
-                    // rows past the sequence end may hold anything: zero V there (K rows are masked)
+                    // rows past the sequence end may hold anything: zero V there (K rows
+                    // are masked); V is [page][half][16 rows][128 bytes]
                     const int zrows = KT - nv;
                     for (int e = lane; e < 2 * zrows * 8; e += 32) {
                         const int hf = e / (zrows * 8);
                         const int r = nv + (e / 8) % zrows;
                         const int ch = e % 8;
-                        *reinterpret_cast<uint4*>(dst + hf * (KT * 128) + r * 128 + ch * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vt + (r >> 4) * 4096 + hf * 2048 + (r & 15) * 128 +
+                                                  ch * 16) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();  // the tensor core reads V through the async proxy
                     __syncwarp();
@@ -412,7 +422,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 const uint32_t va = sbase + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
-                    const uint64_t bd = smem_desc_sw128(va + kk * 2048, KT * 128, 1024);
+                    const uint64_t bd = smem_desc_sw128(va + kk * 4096, 2048, 1024);
                     tc_mma_bf16_ts_elect(tO, pa + kk * 8, bd, IDESC_PV, (j == 0 && kk == 0) ? 0u : 1u);
                 }
                 tc_commit_elect(&kempty[s]);
@@ -774,7 +784,7 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     if (rows >= (1LL << 31)) return TV_ERR_UNSUPPORTED;
     CUtensorMap qm, km, vm;
     if (!make_q_map(&qm, a.q, D, a.Hq, (int64_t)a.B * a.N, G, npt) ||
-        !make_cache_map(&km, a.k_cache, D, rows) || !make_cache_map(&vm, a.v_cache, D, rows))
+        !make_cache_map(&km, a.k_cache, D, rows) || !make_page_map(&vm, a.v_cache, rows))
         return TV_ERR_CUDA;
     Params prm{};
     prm.table = a.block_table;

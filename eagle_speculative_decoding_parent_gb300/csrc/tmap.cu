@@ -41,6 +41,19 @@ bool make_cache_map(CUtensorMap* map, const void* base, int d, int64_t rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_page_map(CUtensorMap* map, const void* base, int64_t rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    // (column in half, row, half): a box is one 16-row page, both 64-column halves
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, 2};
+    cuuint64_t strides[2] = {256, 128};
+    cuuint32_t box[3] = {64, 16, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_q_map(CUtensorMap* map, const void* base, int d, int Hq, int64_t nodes, int G,
                 int npt) {
     EncodeTiledFn enc = encode_fn();
