@@ -1,21 +1,29 @@
-// tree_accept: one thread-block cluster per sequence.
+// tree_accept kernels.
 //
-// Each CTA of the cluster owns a contiguous slice of the vocabulary.  Only
-// the rows the acceptance rule needs are read:
-//   greedy      a level-by-level walk from the root: the argmax of every row
-//               on the current frontier of fully matching nodes (usually one)
-//               is reduced inside each CTA, exchanged through distributed
-//               shared memory, and the matching children form the next
-//               frontier; the walk stops at the deepest accepted level, whose
-//               argmax is the bonus token.  Rows read ~ accepted depth + 1.
-//   stochastic  the accept tests touch two scalars per draft; only the row(s)
-//               the emitted token is drawn from are read: integer weights
-//               (exact sums, so the draw does not depend on summation order),
-//               slice sums exchanged across the cluster, and the CTA holding
-//               the target prefix sum scans its slice.
-// All CTAs of a cluster take identical control-flow decisions (they read the
-// same inputs and the same exchanged values), so every cluster barrier is
-// reached by every CTA.
+//   greedy walk   (large batches) one thread-block cluster per sequence; each
+//                 CTA owns a slice of the vocabulary.  A level-by-level walk
+//                 from the root: the argmax of every row on the current
+//                 frontier of fully matching nodes (usually one) is reduced
+//                 inside each CTA, exchanged through distributed shared memory,
+//                 and the matching children form the next frontier; the walk
+//                 stops at the deepest accepted level, whose argmax is the bonus
+//                 token.  Rows read ~ accepted depth + 1.
+//   greedy rows   (small batches) every row's argmax in parallel: each row is
+//                 cut into chunks, one CTA per chunk; partial results go to the
+//                 workspace, the CTA that completes a row (arrival counter)
+//                 reduces it, and the CTA that completes a sequence walks its
+//                 tree.  Reads every row once, without the walk's latency.
+//   stochastic    the accept tests touch two scalars per draft (all evaluated at
+//                 once, the first failure wins); only the row(s) the emitted
+//                 token is drawn from are read, cut into chunks, one CTA per
+//                 chunk.  Integer weights make the sums exact (the draw does not
+//                 depend on summation order); the CTA that completes a sequence
+//                 picks the chunk holding the target prefix sum and searches it.
+// Cluster kernels: all CTAs of a cluster take identical control-flow decisions
+// (same inputs, same exchanged values), so every cluster barrier is reached by
+// every CTA.  Arrival counters return to zero when a call completes.
+#include <algorithm>
+
 #include <cooperative_groups.h>
 
 #include "tv_device.cuh"
@@ -62,11 +70,16 @@ __device__ __forceinline__ void take(ArgBest& a, float x, int i) {
     a.i = better ? i : a.i;
 }
 
+// Four consecutive elements i..i+3 at once: one maximum, and only when it
+// beats the running best (or is the first non-NaN value seen) the lowest
+// component equal to it is located.  Same result as four take() calls
+// (NaNs skipped, ties to the lower index), at a fraction of the instructions.
 __device__ __forceinline__ void take4(ArgBest& a, const float4& x, int i) {
-    take(a, x.x, i);
-    take(a, x.y, i + 1);
-    take(a, x.z, i + 2);
-    take(a, x.w, i + 3);
+    const float m = fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w));
+    if (m > a.v || (a.i == NO_INDEX && m == m)) {
+        a.v = m;
+        a.i = i + ((x.x == m) ? 0 : (x.y == m) ? 1 : (x.z == m) ? 2 : 3);
+    }
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), written from the published
@@ -89,11 +102,17 @@ __device__ __forceinline__ uint4 draw(const AccParams& p, int b, int k) {
                          make_uint2((uint32_t)p.seed, (uint32_t)(p.seed >> 32)));
 }
 
-// Fixed-point weight floor(min(x, 1) * 2^40); 0 for NaN and x <= 0.
+// Fixed-point weight floor(min(x, 1) * 2^40); 0 for NaN and x <= 0.  Taken
+// from the bits with integer shifts (x * 2^40 = mantissa * 2^(exponent - 110)),
+// which equals the truncating float-to-integer conversion of x * 2^40 but
+// stays off the slow 64-bit conversion path.
 __device__ __forceinline__ uint64_t weight(float x) {
-    if (!(x > 0.f)) return 0ull;
-    if (x >= 1.f) return 1ull << 40;
-    return __float2ull_rz(__fmul_rn(x, 1099511627776.f));
+    const uint32_t u = __float_as_uint(x);
+    if ((int32_t)u <= 0) return 0ull;                                  // +0, negative, -NaN
+    if (u >= 0x3F800000u) return (u > 0x7F800000u) ? 0ull : (1ull << 40);  // NaN; >= 1
+    const int sh = (int)(u >> 23) - 110;
+    const uint64_t m = (uint64_t)((u & 0x7FFFFFu) | 0x800000u);
+    return (sh >= 0) ? (m << sh) : (sh > -24 ? (m >> -sh) : 0ull);
 }
 
 __device__ __forceinline__ uint64_t elem_weight(const float* a, const float* bq, int t, bool resid) {
@@ -158,80 +177,6 @@ __device__ ArgBest block_argmax(const float* __restrict__ row, int lo, int hi, A
     return r;
 }
 
-// Sum of integer weights over this CTA's slice, per warp segment (kept in
-// wsum[]) and in total.  resid: weight(a - b); otherwise weight(a).
-__device__ uint64_t slice_weight_sum(const float* a, const float* bq, bool resid, const Slice& s,
-                                     uint64_t* wsum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int slo = min(s.hi, s.lo + warp * s.seg), shi = min(s.hi, slo + s.seg);
-    uint64_t acc = 0;
-    const bool vec = ((reinterpret_cast<uintptr_t>(a + slo) | (bq ? reinterpret_cast<uintptr_t>(bq + slo) : 0)) & 15) == 0;
-    int t = slo;
-    if (vec) {
-        // four floats per lane per step, four steps in flight
-        const int nv4 = (shi - slo) >> 2;
-        const float4* a4 = reinterpret_cast<const float4*>(a + slo);
-        const float4* b4 = resid ? reinterpret_cast<const float4*>(bq + slo) : nullptr;
-        auto wsum4 = [&](const float4& x, const float4& y) -> uint64_t {
-            if (resid)
-                return weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
-                       weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
-            return weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
-        };
-        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        int e = lane;
-        // four independent loads per operand in flight before any use
-        for (; e + 96 < nv4; e += 128) {
-            const float4 x0 = __ldg(a4 + e), x1 = __ldg(a4 + e + 32);
-            const float4 x2 = __ldg(a4 + e + 64), x3 = __ldg(a4 + e + 96);
-            const float4 y0 = resid ? __ldg(b4 + e) : zero4, y1 = resid ? __ldg(b4 + e + 32) : zero4;
-            const float4 y2 = resid ? __ldg(b4 + e + 64) : zero4, y3 = resid ? __ldg(b4 + e + 96) : zero4;
-            acc += wsum4(x0, y0) + wsum4(x1, y1) + wsum4(x2, y2) + wsum4(x3, y3);
-        }
-        for (; e < nv4; e += 32) acc += wsum4(__ldg(a4 + e), resid ? __ldg(b4 + e) : zero4);
-        t = slo + 4 * nv4;
-    }
-    for (t += lane; t < shi; t += 32) acc += elem_weight(a, bq, t, resid);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    __syncthreads();
-    if (lane == 0) wsum[warp] = acc;
-    __syncthreads();
-    uint64_t tot = 0;
-    for (int w = 0; w < ACC_WARPS; ++w) tot += wsum[w];
-    return tot;
-}
-
-// Within this CTA's slice, the smallest index whose inclusive prefix sum of
-// weights exceeds T (0 <= T < slice sum).  Run by one warp; returns in lane 0.
-__device__ int slice_find(const float* a, const float* bq, bool resid, const Slice& s,
-                          const uint64_t* wsum, uint64_t T) {
-    const int lane = threadIdx.x & 31;
-    int w = 0;
-    while (w < ACC_WARPS - 1 && T >= wsum[w]) {
-        T -= wsum[w];
-        ++w;
-    }
-    const int slo = min(s.hi, s.lo + w * s.seg), shi = min(s.hi, slo + s.seg);
-    for (int base = slo; base < shi; base += 32) {
-        const int t = base + lane;
-        uint64_t x = (t < shi) ? elem_weight(a, bq, t, resid) : 0ull;
-        // inclusive warp scan
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        const uint64_t chunk = __shfl_sync(0xffffffffu, x, 31);
-        if (T < chunk) {
-            const unsigned hit = __ballot_sync(0xffffffffu, x > T);
-            return base + __ffs(hit) - 1;
-        }
-        T -= chunk;
-    }
-    return -1;  // not reached when T < slice sum
-}
-
 __device__ void write_fail(const AccParams& p, int b, int st) {
     for (int j = threadIdx.x; j < p.max_path; j += blockDim.x) {
         p.path[(int64_t)b * p.max_path + j] = (j == 0) ? 0 : -1;
@@ -278,17 +223,19 @@ __device__ void write_path(const AccParams& p, int b, const int* spar, const int
 }
 
 // Tree and token checks in the order the acceptance rule states them
-// (structure first, then token range).  One thread.
+// (structure first, then token range).  One full warp; result in every lane.
 __device__ int check_inputs(const int* spar, const int* stok, int N, int V, bool chain) {
-    for (int i = 0; i < N; ++i) {
+    const int lane = threadIdx.x & 31;
+    bool tree_bad = false, chain_bad = false, tok_bad = false;
+    for (int i = lane; i < N; i += 32) {
         const int pa = spar[i];
-        if ((i == 0 && pa != -1) || (i > 0 && (pa < 0 || pa >= i))) return TV_ERR_BAD_TREE;
+        tree_bad |= (i == 0 && pa != -1) || (i > 0 && (pa < 0 || pa >= i));
+        chain_bad |= (i > 0 && pa != i - 1);
+        tok_bad |= (i > 0 && (stok[i] < 0 || stok[i] >= V));
     }
-    if (chain)
-        for (int i = 1; i < N; ++i)
-            if (spar[i] != i - 1) return TV_ERR_UNSUPPORTED;
-    for (int i = 1; i < N; ++i)
-        if (stok[i] < 0 || stok[i] >= V) return TV_ERR_OUT_OF_RANGE;
+    if (__any_sync(0xffffffffu, tree_bad)) return TV_ERR_BAD_TREE;
+    if (chain && __any_sync(0xffffffffu, chain_bad)) return TV_ERR_UNSUPPORTED;
+    if (__any_sync(0xffffffffu, tok_bad)) return TV_ERR_OUT_OF_RANGE;
     return TV_OK;
 }
 
@@ -312,7 +259,10 @@ accept_greedy_kernel(AccParams p) {
         sam[tid] = -1;
     }
     __syncthreads();
-    if (tid == 0) sflag = check_inputs(spar, stok, N, p.V, false);
+    if (tid < 32) {
+        const int f = check_inputs(spar, stok, N, p.V, false);
+        if (tid == 0) sflag = f;
+    }
     __syncthreads();
     if (sflag != TV_OK) {
         if (rank == 0) write_fail(p, b, sflag);
@@ -380,34 +330,126 @@ accept_greedy_kernel(AccParams p) {
     }
 }
 
-// Greedy acceptance for small batches: every row's argmax is computed in
-// parallel (one cluster per row, DSMEM reduction), written to the workspace,
-// and the CTA that completes a sequence's last row (atomic ticket) walks the
-// tree.  Reads every row once, but without the walk's level-by-level latency.
+constexpr int CH_THREADS = 256;            // CTA size of the chunked kernels
+constexpr int CH_WARPS = CH_THREADS / 32;
+constexpr int CH_MAX = 128;                // chunks per row at most
+constexpr int FIND_TILES = 512;            // 256-element tiles a chunk search holds
+
+// Elements per chunk when a row of V entries is cut into ch chunks (multiple of 4).
+__device__ __host__ __forceinline__ int chunk_len(int V, int ch) {
+    int per = (V + ch - 1) / ch;
+    return (per + 3) & ~3;
+}
+
+// Argmax of row[lo, hi) over the CTA (CH_THREADS threads); valid in every thread.
 template <bool VEC>
-__global__ void __launch_bounds__(ACC_THREADS)
-accept_rowscan_kernel(AccParams p, int32_t* __restrict__ am_ws, int32_t* __restrict__ tickets) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int S = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
+__device__ ArgBest chunk_argmax(const float* __restrict__ row, int lo, int hi, ArgBest* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    ArgBest a{-INFINITY, NO_INDEX};
+    if (VEC) {
+        const int nv = (hi - lo) >> 2;
+        const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+        constexpr int T = CH_THREADS;
+        int e = tid;
+        for (; e + 3 * T < nv; e += 4 * T) {
+            const float4 x0 = __ldg(r4 + e), x1 = __ldg(r4 + e + T);
+            const float4 x2 = __ldg(r4 + e + 2 * T), x3 = __ldg(r4 + e + 3 * T);
+            take4(a, x0, lo + 4 * e);
+            take4(a, x1, lo + 4 * (e + T));
+            take4(a, x2, lo + 4 * (e + 2 * T));
+            take4(a, x3, lo + 4 * (e + 3 * T));
+        }
+        for (; e < nv; e += T) take4(a, __ldg(r4 + e), lo + 4 * e);
+        for (int i = lo + 4 * nv + tid; i < hi; i += T) take(a, __ldg(row + i), i);
+    } else {
+        for (int i = lo + tid; i < hi; i += CH_THREADS) take(a, __ldg(row + i), i);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, a.v, off);
+        const int j = __shfl_xor_sync(0xffffffffu, a.i, off);
+        if (beats(w, j, a.v, a.i)) {
+            a.v = w;
+            a.i = j;
+        }
+    }
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    ArgBest r = red[0];
+    for (int w = 1; w < CH_WARPS; ++w)
+        if (beats(red[w].v, red[w].i, r.v, r.i)) r = red[w];
+    return r;
+}
+
+// Walks sequence b's tree given every row's argmax (sam[], -1 for none) and
+// writes the result: accepted(c) = accepted(parent) and token(c) == argmax of
+// the parent's row; the deepest accepted node is emitted with its argmax.
+__device__ void walk_and_write(const AccParams& p, int b, const int* spar, const int* stok,
+                               const int* sam) {
+    __shared__ int schosen;
+    const int N = p.N;
+    if (threadIdx.x < 32) {
+        // node c is accepted when every edge on its root path matches; lane takes
+        // nodes lane and lane + 32: key = depth, then the lower index on ties
+        const int lane = threadIdx.x;
+        int best = -1;
+        for (int c = lane; c < N; c += 32) {
+            bool acc = true;
+            int d = 0;
+            for (int j = c; j > 0; j = spar[j], ++d) {
+                const int pj = spar[j];
+                acc = acc && sam[pj] >= 0 && stok[j] == sam[pj];
+            }
+            if (acc) best = max(best, (d << 8) | (255 - c));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, off));
+        if (lane == 0) schosen = 255 - (best & 255);
+    }
+    __syncthreads();
+    const int chosen = schosen;
+    if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+    else write_path(p, b, spar, stok, chosen, sam[chosen]);
+}
+
+// Greedy acceptance, every row in parallel: CTA (row, c) takes chunk c of the
+// row; ws: part[row][CH_MAX] (value bits, index), am[row], row_tick[row],
+// seq_tick[b].
+template <bool VEC>
+__global__ void __launch_bounds__(CH_THREADS)
+accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __restrict__ am,
+                   int32_t* __restrict__ row_tick, int32_t* __restrict__ seq_tick) {
     pdl_launch_dependents();
     pdl_wait();
-    const int cl = blockIdx.x / S;
     const int N = p.N;
-    const int b = cl / N, row = cl % N;
+    const int row = blockIdx.x / ch, c = blockIdx.x % ch;
+    const int b = row / N;
     const int tid = threadIdx.x;
-    __shared__ ArgBest red[ACC_WARPS];
-    __shared__ ArgBest exch;
+    __shared__ ArgBest red[CH_WARPS];
     __shared__ int last;
     __shared__ int spar[64], stok[64], sam[64];
     __shared__ int sflag;
-    const Slice sl = make_slice(p.V, S, rank);
-    const ArgBest a = block_argmax<VEC>(p.target + ((int64_t)b * N + row) * p.V, sl.lo, sl.hi, red);
-    if (tid == 0) exch = a;
-    cluster.sync();
-    if (rank == 0 && tid < 32) {
+    const int per = chunk_len(p.V, ch);
+    const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
+    const ArgBest a = chunk_argmax<VEC>(p.target + (int64_t)row * p.V, lo, hi, red);
+    if (tid == 0) {
+        part[(int64_t)row * CH_MAX + c] = make_int2(__float_as_int(a.v), a.i);
+        __threadfence();
+        last = (atomicAdd(&row_tick[row], 1) == ch - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    // this CTA completed the row: reduce its chunks
+    __threadfence();
+    if (tid < 32) {
         ArgBest x{-INFINITY, NO_INDEX};
-        if (tid < S) x = *cluster.map_shared_rank(&exch, tid);
+        for (int k = tid; k < ch; k += 32) {
+            const int2 v = __ldcg(part + (int64_t)row * CH_MAX + k);
+            if (v.y != NO_INDEX && beats(__int_as_float(v.x), v.y, x.v, x.i)) {
+                x.v = __int_as_float(v.x);
+                x.i = v.y;
+            }
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
@@ -418,13 +460,12 @@ accept_rowscan_kernel(AccParams p, int32_t* __restrict__ am_ws, int32_t* __restr
             }
         }
         if (tid == 0) {
-            am_ws[(int64_t)b * N + row] = (x.i == NO_INDEX) ? -1 : x.i;
+            am[row] = (x.i == NO_INDEX) ? -1 : x.i;
+            row_tick[row] = 0;  // leave the workspace ready for the next call
             __threadfence();
-            last = (atomicAdd(&tickets[b], 1) == N - 1);
+            last = (atomicAdd(&seq_tick[b], 1) == N - 1);
         }
     }
-    cluster.sync();  // peers' exchange slots stay alive until rank 0 has read them
-    if (rank != 0) return;
     __syncthreads();
     if (!last) return;
     // this CTA completed sequence b: walk its tree
@@ -432,137 +473,307 @@ accept_rowscan_kernel(AccParams p, int32_t* __restrict__ am_ws, int32_t* __restr
     if (tid < N) {
         spar[tid] = p.parents[(int64_t)b * N + tid];
         stok[tid] = p.tokens[(int64_t)b * N + tid];
-        sam[tid] = __ldcg(am_ws + (int64_t)b * N + tid);
+        sam[tid] = __ldcg(am + (int64_t)b * N + tid);
     }
     __syncthreads();
-    if (tid == 0) {
-        tickets[b] = 0;  // leave the workspace ready for the next call
-        sflag = check_inputs(spar, stok, N, p.V, false);
+    if (tid < 32) {
+        const int f = check_inputs(spar, stok, N, p.V, false);
+        if (tid == 0) {
+            seq_tick[b] = 0;
+            sflag = f;
+        }
     }
     __syncthreads();
     if (sflag != TV_OK) {
         write_fail(p, b, sflag);
         return;
     }
-    __shared__ int schosen;
-    if (tid == 0) {
-        // accepted(c) = accepted(parent) and token(c) == argmax(parent row); topological order
-        uint64_t acc = 1ull;
-        int dep[64];
-        dep[0] = 0;
-        int chosen = 0;
-        for (int c = 1; c < N; ++c) {
-            const int pc = spar[c];
-            dep[c] = dep[pc] + 1;
-            if (((acc >> pc) & 1ull) && sam[pc] >= 0 && stok[c] == sam[pc]) {
-                acc |= 1ull << c;
-                if (dep[c] > dep[chosen]) chosen = c;
-            }
-        }
-        schosen = chosen;
-    }
-    __syncthreads();
-    const int chosen = schosen;
-    if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
-    else write_path(p, b, spar, stok, chosen, sam[chosen]);
+    walk_and_write(p, b, spar, stok, sam);
 }
 
-__global__ void __launch_bounds__(ACC_THREADS)
-accept_stochastic_kernel(AccParams p) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-    pdl_launch_dependents();
-    pdl_wait();
-    const int b = blockIdx.x / C;
-    __shared__ int spar[64], stok[64];
-    __shared__ uint64_t wsum[ACC_WARPS];
-    __shared__ uint64_t xsum[2];   // this CTA's slice sum, per attempt
-    __shared__ int xidx;           // token found by this CTA (-1: none)
-    __shared__ int sflag;
-    const int tid = threadIdx.x, N = p.N;
-    if (tid == 0) {
-        sflag = 0;
-        xidx = -1;
+// Sum of integer weights over row a's chunk [lo, hi): weight(a - b) when b
+// is given (the residual), weight(a) otherwise; valid in thread 0.
+template <bool VEC>
+__device__ uint64_t chunk_weight_sum(const float* a, const float* bq, int lo, int hi,
+                                     uint64_t* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool resid = bq != nullptr;
+    uint64_t w = 0;
+    int i = lo;
+    if (VEC) {
+        const int nv = (hi - lo) >> 2;
+        const float4* a4 = reinterpret_cast<const float4*>(a + lo);
+        const float4* b4 = resid ? reinterpret_cast<const float4*>(bq + lo) : nullptr;
+        constexpr int T = CH_THREADS;
+        auto acc4 = [&](const float4& x, const float4& y) {
+            if (resid)
+                w += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
+                     weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
+            else
+                w += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
+        };
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        int e = tid;
+        for (; e + 3 * T < nv; e += 4 * T) {
+            const float4 x0 = __ldg(a4 + e), x1 = __ldg(a4 + e + T);
+            const float4 x2 = __ldg(a4 + e + 2 * T), x3 = __ldg(a4 + e + 3 * T);
+            const float4 y0 = resid ? __ldg(b4 + e) : z4, y1 = resid ? __ldg(b4 + e + T) : z4;
+            const float4 y2 = resid ? __ldg(b4 + e + 2 * T) : z4;
+            const float4 y3 = resid ? __ldg(b4 + e + 3 * T) : z4;
+            acc4(x0, y0);
+            acc4(x1, y1);
+            acc4(x2, y2);
+            acc4(x3, y3);
+        }
+        for (; e < nv; e += T) acc4(__ldg(a4 + e), resid ? __ldg(b4 + e) : z4);
+        i = lo + 4 * nv;
+    }
+    for (i += tid; i < hi; i += CH_THREADS) w += elem_weight(a, bq, i, resid);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+    __syncthreads();  // red may still be read from an earlier call
+    if (lane == 0) red[warp] = w;
+    __syncthreads();
+    uint64_t tot = 0;
+    for (int k = 0; k < CH_WARPS; ++k) tot += red[k];
+    return tot;
+}
+
+// Picks the chunk holding the draw: per-chunk sums v(k) (k < ch) come from
+// `get`; one full warp; returns the chunk (-1 when the total is zero) and the
+// remaining offset T inside it, in every lane.
+template <typename Get>
+__device__ int pick_chunk(int ch, uint32_t x1, Get get, uint64_t& T, uint64_t& total) {
+    const int lane = threadIdx.x & 31;
+    uint64_t v[CH_MAX / 32];
+    uint64_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < CH_MAX / 32; ++q) {
+        const int k = lane + 32 * q;
+        v[q] = (k < ch) ? get(k) : 0ull;
+        tot += v[q];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    total = tot;
+    T = 0;
+    if (tot == 0) return -1;
+    const uint64_t hi = __umul64hi((uint64_t)x1, tot), lo = (uint64_t)x1 * tot;
+    uint64_t t = (hi << 32) | (lo >> 32);
+    // chunk order k = 32 q + lane: scan each group of 32 in turn
+#pragma unroll
+    for (int q = 0; q < CH_MAX / 32; ++q) {
+        uint64_t x = v[q];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        const uint64_t grp = __shfl_sync(0xffffffffu, x, 31);
+        if (t < grp) {
+            const int l = __ffs(__ballot_sync(0xffffffffu, x > t)) - 1;
+            T = t - __shfl_sync(0xffffffffu, x - v[q], l);
+            return 32 * q + l;
+        }
+        t -= grp;
+    }
+    return -1;  // not reached: t < total
+}
+
+// Smallest index i in [lo, hi) whose inclusive prefix sum of weights (from lo)
+// exceeds T, for T below the range's sum; the whole CTA searches, the result
+// is valid in thread 0.  Level 1: sums of 256-element tiles (one warp per
+// tile); level 2: one warp scans the tile sums, then the chosen tile's
+// elements, eight per lane.
+__device__ int chunk_find(const float* a, const float* bq, int lo, int hi, uint64_t T,
+                          uint64_t* tsum /* [>= ceil((hi-lo)/256)] */) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool resid = bq != nullptr;
+    constexpr int TILE = 256;
+    const int nt = (hi - lo + TILE - 1) / TILE;
+    for (int t = warp; t < nt; t += CH_WARPS) {
+        const int base = lo + t * TILE + lane * 8;
+        uint64_t acc = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (base + k < hi) acc += elem_weight(a, bq, base + k, resid);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) tsum[t] = acc;
     }
     __syncthreads();
+    __shared__ int sfound;
+    if (warp == 0) {
+        // tile containing T: lane-strided partial sums, then a warp scan
+        int tile = -1;
+        uint64_t rem = T;
+        for (int t0 = 0; t0 < nt && tile < 0; t0 += 32) {
+            const uint64_t v = (t0 + lane < nt) ? tsum[t0 + lane] : 0ull;
+            uint64_t x = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            const uint64_t tot = __shfl_sync(0xffffffffu, x, 31);
+            if (rem < tot) {
+                const unsigned hit = __ballot_sync(0xffffffffu, x > rem);
+                const int l = __ffs(hit) - 1;
+                const uint64_t before = __shfl_sync(0xffffffffu, x - v, l);
+                tile = t0 + l;
+                rem -= before;
+            } else {
+                rem -= tot;
+            }
+        }
+        int found = -1;
+        if (tile >= 0) {
+            // eight consecutive elements per lane, a warp scan over the lane sums
+            const int base = lo + tile * TILE + lane * 8;
+            uint64_t wv[8];
+            uint64_t ls = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                wv[k] = (base + k < hi) ? elem_weight(a, bq, base + k, resid) : 0ull;
+                ls += wv[k];
+            }
+            uint64_t x = ls;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, x > rem);
+            const int l = __ffs(hit) - 1;
+            if (lane == l) {
+                uint64_t run = x - ls;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    run += wv[k];
+                    if (found < 0 && run > rem) found = base + k;
+                }
+            }
+            found = __shfl_sync(0xffffffffu, found, l < 0 ? 0 : l);
+        }
+        if (lane == 0) sfound = found;
+    }
+    __syncthreads();
+    return sfound;
+}
+
+// Stochastic chain acceptance: CTA (b, c) takes chunk c of the row the token
+// is drawn from; ws: sums[b][CH_MAX] (weight sum of the chunk), seq_tick[b].
+template <bool VEC>
+__global__ void __launch_bounds__(CH_THREADS)
+accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
+                         int32_t* __restrict__ seq_tick) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x / ch, c = blockIdx.x % ch;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
+    __shared__ int spar[64], stok[64];
+    __shared__ int sflag, skstar, last;
+    __shared__ uint64_t red[CH_WARPS];
+    __shared__ uint64_t tsum[FIND_TILES];
     if (tid < N) {
         spar[tid] = p.parents[(int64_t)b * N + tid];
         stok[tid] = p.tokens[(int64_t)b * N + tid];
     }
     __syncthreads();
-    if (tid == 0) sflag = check_inputs(spar, stok, N, p.V, true);
+    if (tid < 32) {
+        const int f = check_inputs(spar, stok, N, p.V, true);
+        if (tid == 0) sflag = f;
+    }
     __syncthreads();
     if (sflag != TV_OK) {
-        if (rank == 0) write_fail(p, b, sflag);
-        return;
+        if (c == 0) write_fail(p, b, sflag);
+        return;  // every CTA of the sequence returns here: its counter is untouched
     }
-    // accept tests (every CTA, redundantly: a few scalars)
+    // accept tests k = 1..K, all at once (counter-based draws); the first failure wins
     const int K = N - 1;
-    int kstar = K + 1;  // first rejected position, K+1 = none
-    for (int k = 1; k <= K; ++k) {
-        const uint4 w = draw(p, b, k);
-        const uint32_t u24 = w.x >> 8;
-        const int x = stok[k];
-        const float pk = __ldg(p.target + ((int64_t)b * N + (k - 1)) * p.V + x);
-        const float qk = __ldg(p.draft + ((int64_t)b * N + k) * p.V + x);
-        const bool acc = __dmul_rn((double)u24, (double)qk) < __dmul_rn((double)pk, 16777216.0);
-        if (!acc) {
-            kstar = k;
-            break;
+    if (warp == 0) {
+        int kst = K + 1;  // first rejected position, K+1 = none
+        for (int k0 = 1; k0 <= K && kst > K; k0 += 32) {
+            const int k = k0 + lane;
+            bool acc = true;
+            if (k <= K) {
+                const uint32_t u24 = draw(p, b, k).x >> 8;
+                const int x = stok[k];
+                const float pk = __ldg(p.target + ((int64_t)b * N + (k - 1)) * p.V + x);
+                const float qk = __ldg(p.draft + ((int64_t)b * N + k) * p.V + x);
+                acc = __dmul_rn((double)u24, (double)qk) < __dmul_rn((double)pk, 16777216.0);
+            }
+            const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+            if (rej) kst = k0 + __ffs(rej) - 1;
         }
+        if (lane == 0) skstar = kst;
     }
+    __syncthreads();
+    const int kstar = skstar;
     const bool rejected = kstar <= K;
     const float* rowa = p.target + ((int64_t)b * N + (rejected ? kstar - 1 : K)) * p.V;
     const float* rowb = rejected ? p.draft + ((int64_t)b * N + kstar) * p.V : nullptr;
+    const int per = chunk_len(p.V, ch);
+    {
+        const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
+        const uint64_t mine = chunk_weight_sum<VEC>(rowa, rowb, lo, hi, red);
+        if (tid == 0) {
+            sums[(int64_t)b * CH_MAX + c] = mine;
+            __threadfence();
+            last = (atomicAdd(&seq_tick[b], 1) == ch - 1);
+        }
+    }
+    __syncthreads();
+    if (!last) return;
+    // this CTA completed sequence b: pick the chunk holding the draw
+    __threadfence();
+    __shared__ int schunk, sresid;
+    __shared__ uint64_t sT, stot;
+    __shared__ uint64_t fsum[CH_MAX];
     const uint32_t x1 = draw(p, b, rejected ? kstar : K + 1).y;
-    const Slice sl = make_slice(p.V, C, rank);
-
-    bool resid = rejected;
-    int token = -1;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const uint64_t mine = slice_weight_sum(rowa, rowb, resid, sl, wsum);
-        if (tid == 0) xsum[attempt] = mine;
-        cluster.sync();
-        uint64_t S = 0, before = 0;
-        for (int r = 0; r < C; ++r) {
-            const uint64_t v = *cluster.map_shared_rank(&xsum[attempt], r);
-            if (r < rank) before += v;
-            S += v;
+    if (warp == 0) {
+        uint64_t T, tot;
+        const int cc = pick_chunk(ch, x1, [&](int k) { return __ldcg(sums + (int64_t)b * CH_MAX + k); },
+                                  T, tot);
+        if (lane == 0) {
+            seq_tick[b] = 0;  // leave the workspace ready for the next call
+            schunk = cc;
+            sT = T;
+            stot = tot;
+            sresid = rejected;
         }
-        if (S == 0) {
-            if (resid) {
-                resid = false;  // residual has no mass: draw from the target row itself
-                continue;
-            }
-            break;  // zero-mass target row
-        }
-        const uint64_t hi = __umul64hi((uint64_t)x1, S), lo = (uint64_t)x1 * S;
-        const uint64_t T = (hi << 32) | (lo >> 32);
-        if (T >= before && T < before + mine && tid < 32) {
-            const int t = slice_find(rowa, rowb, resid, sl, wsum, T - before);
-            if (tid == 0) xidx = t;
-        }
-        cluster.sync();
-        if (rank == 0) {
-            for (int r = 0; r < C; ++r) {
-                const int v = *cluster.map_shared_rank(&xidx, r);
-                if (v >= 0) token = v;
-            }
-        }
-        break;
     }
-    cluster.sync();  // exchange slots stay alive until every CTA has read them
-    if (rank == 0) {
-        __shared__ int stoken;
-        if (tid == 0) stoken = token;
+    __syncthreads();
+    if (rejected && stot == 0) {
+        // the residual has no mass: draw from the target row itself (rare: this
+        // CTA sums every chunk of it)
+        for (int k = 0; k < ch; ++k) {
+            const int lo = min(p.V, k * per), hi = min(p.V, lo + per);
+            const uint64_t v = chunk_weight_sum<VEC>(rowa, nullptr, lo, hi, red);
+            if (tid == 0) fsum[k] = v;
+        }
         __syncthreads();
-        if (stoken < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
-        else write_path(p, b, spar, stok, rejected ? kstar - 1 : K, stoken);
+        if (warp == 0) {
+            uint64_t T, tot;
+            const int cc = pick_chunk(ch, x1, [&](int k) { return fsum[k]; }, T, tot);
+            if (lane == 0) {
+                schunk = cc;
+                sT = T;
+                sresid = 0;
+            }
+        }
+        __syncthreads();
     }
+    int token = -1;
+    if (schunk >= 0) {
+        const int lo = min(p.V, schunk * per), hi = min(p.V, lo + per);
+        token = chunk_find(rowa, sresid ? rowb : nullptr, lo, hi, sT, tsum);
+    }
+    if (token < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+    else write_path(p, b, spar, stok, rejected ? kstar - 1 : K, token);
 }
 
-// Allows 16-CTA clusters for every kernel here when the device supports it.
+// Allows 16-CTA clusters for the walk kernels when the device supports it.
 bool enable_large_clusters() {
     static int state = -1;
     if (state < 0) {
@@ -570,12 +781,6 @@ bool enable_large_clusters() {
         bool ok = cudaFuncSetAttribute(accept_greedy_kernel<true>,
                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         ok = ok && cudaFuncSetAttribute(accept_greedy_kernel<false>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        ok = ok && cudaFuncSetAttribute(accept_rowscan_kernel<true>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        ok = ok && cudaFuncSetAttribute(accept_rowscan_kernel<false>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        ok = ok && cudaFuncSetAttribute(accept_stochastic_kernel,
                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
         if (ok) {
             cudaLaunchConfig_t cfg = {};
@@ -598,13 +803,7 @@ bool enable_large_clusters() {
     return state == 1;
 }
 
-int pow2_at_least(int64_t x) {
-    int c = 1;
-    while (c < x && c < 16) c <<= 1;
-    return c;
-}
-
-// Row-scan pays for every row once at full bandwidth; the walk pays a few
+// The row scan pays for every row once at full bandwidth; the walk pays a few
 // microseconds of latency per tree level (at most 8 levels assumed).
 bool prefer_rowscan(int B, int N, int V) {
     const double bytes = (double)B * N * V * 4.0;
@@ -615,11 +814,38 @@ bool prefer_rowscan(int B, int N, int V) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Chunks per row: about four CTAs per multiprocessor over `rows` rows, at
+// least 1024 elements a chunk, and few enough that a chunk search fits.
+int chunks_for(int64_t rows, int V, int sms) {
+    int64_t ch = (4LL * sms + rows - 1) / rows;
+    ch = std::min<int64_t>(ch, std::max(1, V / 1024));
+    const int64_t need = ((int64_t)V + 256LL * FIND_TILES - 1) / (256LL * FIND_TILES);
+    ch = std::max<int64_t>(ch, need);
+    return (int)std::min<int64_t>(std::max<int64_t>(ch, 1), CH_MAX);
+}
+
+struct RowsWs {
+    size_t part, am, row_tick, seq_tick, total;
+};
+RowsWs rows_ws(int B, int N) {
+    const size_t R = (size_t)B * N;
+    RowsWs w;
+    w.part = 0;
+    w.am = w.part + align256(R * CH_MAX * 8);
+    w.row_tick = w.am + align256(R * 4);
+    w.seq_tick = w.row_tick + align256(R * 4);
+    w.total = w.seq_tick + align256((size_t)B * 4);
+    return w;
+}
+size_t stoch_ws_sums(int B) { return align256((size_t)B * CH_MAX * 8); }
+
 }  // namespace
 
 size_t accept_workspace(tv_accept_mode mode, int B, int N, int V) {
-    if (mode != TV_ACCEPT_GREEDY || B <= 0 || !prefer_rowscan(B, N, V)) return 0;
-    return align256((size_t)B * N * 4) + align256((size_t)B * 4);
+    if (B <= 0) return 0;
+    if (mode == TV_ACCEPT_GREEDY)
+        return prefer_rowscan(B, N, V) ? rows_ws(B, N).total : 0;
+    return stoch_ws_sums(B) + align256((size_t)B * 4);
 }
 
 tv_status launch_accept(const AcceptArgs& a) {
@@ -639,40 +865,43 @@ tv_status launch_accept(const AcceptArgs& a) {
     p.out_tokens = a.out_tokens;
     p.max_path = a.max_path;
     p.status = a.status;
-    const bool large = enable_large_clusters();
-    const int cmax = large ? 16 : 8;
     const int sms = device_sm_count();
-    const bool vec = (a.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.target) & 15) == 0);
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.target) & 15) == 0 &&
+                         (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0;
+    const bool vec = (a.V % 4 == 0) && aligned;
     const size_t need = accept_workspace(a.mode, a.B, a.N, a.V);
     if (need > 0 && (a.ws == nullptr || a.ws_bytes < need)) return TV_ERR_WORKSPACE;
-    const bool rowscan = need > 0;
-
-    int C;
-    int64_t units;
-    if (rowscan) {
-        units = (int64_t)a.B * a.N;
-        C = pow2_at_least((2LL * sms + units - 1) / units);
-    } else {
-        units = a.B;
-        C = ((int64_t)a.B * 16 <= 2LL * sms) ? 16 : 8;
-    }
-    if (C > cmax) C = cmax;
-    while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
-    if (units * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
-    LaunchCfg lc(dim3((unsigned)(units * C)), dim3(ACC_THREADS), 0, a.stream, (unsigned)C);
-    const cudaLaunchConfig_t& cfg = lc.cfg;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
     cudaError_t e;
-    if (a.mode == TV_ACCEPT_GREEDY && rowscan) {
-        int32_t* am = static_cast<int32_t*>(a.ws);
-        int32_t* tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.ws) +
-                                                       align256((size_t)a.B * a.N * 4));
-        e = vec ? cudaLaunchKernelEx(&cfg, accept_rowscan_kernel<true>, p, am, tickets)
-                : cudaLaunchKernelEx(&cfg, accept_rowscan_kernel<false>, p, am, tickets);
+    if (a.mode == TV_ACCEPT_GREEDY && need > 0) {
+        const int64_t R = (int64_t)a.B * a.N;
+        const int ch = chunks_for(R, a.V, sms);
+        if (R * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+        const RowsWs w = rows_ws(a.B, a.N);
+        int2* part = reinterpret_cast<int2*>(ws + w.part);
+        int32_t* am = reinterpret_cast<int32_t*>(ws + w.am);
+        int32_t* rt = reinterpret_cast<int32_t*>(ws + w.row_tick);
+        int32_t* st = reinterpret_cast<int32_t*>(ws + w.seq_tick);
+        LaunchCfg lc(dim3((unsigned)(R * ch)), dim3(CH_THREADS), 0, a.stream);
+        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<true>, p, ch, part, am, rt, st)
+                : cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<false>, p, ch, part, am, rt, st);
     } else if (a.mode == TV_ACCEPT_GREEDY) {
-        e = vec ? cudaLaunchKernelEx(&cfg, accept_greedy_kernel<true>, p)
-                : cudaLaunchKernelEx(&cfg, accept_greedy_kernel<false>, p);
+        const bool large = enable_large_clusters();
+        int C = ((int64_t)a.B * 16 <= 2LL * sms) ? 16 : 8;
+        if (!large && C > 8) C = 8;
+        while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
+        if ((int64_t)a.B * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+        LaunchCfg lc(dim3((unsigned)(a.B * C)), dim3(ACC_THREADS), 0, a.stream, (unsigned)C);
+        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<true>, p)
+                : cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<false>, p);
     } else {
-        e = cudaLaunchKernelEx(&cfg, accept_stochastic_kernel, p);
+        const int ch = chunks_for(a.B, a.V, sms);
+        if ((int64_t)a.B * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+        uint64_t* sums = reinterpret_cast<uint64_t*>(ws);
+        int32_t* st = reinterpret_cast<int32_t*>(ws + stoch_ws_sums(a.B));
+        LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), 0, a.stream);
+        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<true>, p, ch, sums, st)
+                : cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<false>, p, ch, sums, st);
     }
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }

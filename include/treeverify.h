@@ -171,9 +171,12 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
  * [0, -1, ...] and out_tokens all -1.
  * workspace: at least tree_accept_workspace() bytes (0 means none is needed
  * and NULL is allowed).  Greedy acceptance on small batches reads every row
- * once in parallel and keeps one argmax per row plus a per-sequence arrival
- * counter there; the counters must be zero before the first call (zero the
- * whole buffer once) and every completed call leaves them at zero.
+ * once in parallel, cut into chunks, and keeps per-chunk and per-row argmax
+ * results plus per-row and per-sequence arrival counters there; stochastic
+ * acceptance keeps per-chunk weight sums and a per-sequence arrival counter.
+ * The counters must be zero before the first call (zero the whole buffer
+ * once) and every completed call leaves them at zero; calls sharing one
+ * workspace must not run concurrently.
  * Host errors: N outside [1, 64], V outside [1, 2^24], max_path < 1;
  * TV_ERR_WORKSPACE when the workspace is missing or too small.
  * ------------------------------------------------------------------------ */
