@@ -38,6 +38,8 @@ namespace {
 constexpr int ACC_THREADS = 512;
 constexpr int ACC_WARPS = ACC_THREADS / 32;
 constexpr int NO_INDEX = 0x7fffffff;
+constexpr int TIMED_OUT = -2;      // a row argmax whose data did not arrive in time
+constexpr uint64_t SUM_TIMED_OUT = 1ull << 63;  // a chunk sum whose data did not arrive
 
 struct AccParams {
     const int32_t* parents;
@@ -333,7 +335,6 @@ accept_greedy_kernel(AccParams p) {
 constexpr int CH_THREADS = 256;            // CTA size of the chunked kernels
 constexpr int CH_WARPS = CH_THREADS / 32;
 constexpr int CH_MAX = 128;                // chunks per row at most
-constexpr int FIND_TILES = 512;            // 256-element tiles a chunk search holds
 
 // Elements per chunk when a row of V entries is cut into ch chunks (multiple of 4).
 __device__ __host__ __forceinline__ int chunk_len(int V, int ch) {
@@ -341,26 +342,76 @@ __device__ __host__ __forceinline__ int chunk_len(int V, int ch) {
     return (per + 3) & ~3;
 }
 
+// Rows are streamed through shared memory in pieces of PIECE floats per
+// operand with bulk asynchronous copies, STG pieces in flight per CTA.
+constexpr int PIECE = 2048;
+constexpr int STG = 4;
+
+struct Ring {
+    float* buf;        // [STG][ops][PIECE]
+    uint64_t* full;    // [STG]
+    uint32_t pc;       // pieces this CTA has consumed (ring position and phase)
+};
+
+// Calls f(x, y, i) for x = a[i..i+3] and y = b[i..i+3] (zeros without b), for
+// every i = lo + 4k < hi, each thread a strided subset.  lo and hi - lo are
+// multiples of 4 and the rows 16-byte aligned.  Every thread of the CTA calls
+// it.  Returns false if a piece did not arrive in time (after waiting, with a
+// limit, for the copies still in flight).
+template <typename F>
+__device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring& r, F f) {
+    const int tid = threadIdx.x;
+    const int ops = b ? 2 : 1;
+    const int np = (hi - lo + PIECE - 1) / PIECE;
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int k) {
+        const int s = (int)((r.pc + k) % STG);
+        const int off = lo + k * PIECE;
+        const uint32_t bytes = (uint32_t)min(PIECE, hi - off) * 4u;
+        mbar_arrive_expect_tx(&r.full[s], bytes * ops);
+        bulk_load(r.buf + (size_t)s * ops * PIECE, a + off, bytes, &r.full[s], pol);
+        if (b) bulk_load(r.buf + (size_t)s * ops * PIECE + PIECE, b + off, bytes, &r.full[s], pol);
+    };
+    if (tid == 0)
+        for (int k = 0; k < min(STG, np); ++k) issue(k);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool ok = true;
+    int k = 0;
+    for (; k < np; ++k) {
+        const uint32_t g = r.pc + k;
+        const int s = (int)(g % STG);
+        const bool got = mbar_wait(&r.full[s], (g / STG) & 1u);
+        if (got) {
+            const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
+            const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)s * ops * PIECE);
+            const float4* y4 = x4 + PIECE / 4;
+            for (int e = tid; e < n4; e += blockDim.x) f(x4[e], b ? y4[e] : z4, off + 4 * e);
+        }
+        ok = __syncthreads_and(got) != 0;  // every thread is done with stage s
+        if (!ok) break;
+        if (tid == 0 && k + STG < np) issue(k + STG);
+    }
+    if (!ok && tid == 0) {
+        // let the copies still in flight land before the shared memory is released
+        for (int j = k + 1; j < min(np, k + STG); ++j) {
+            const uint32_t g = r.pc + j;
+            mbar_wait(&r.full[g % STG], (g / STG) & 1u);
+        }
+    }
+    r.pc += np;
+    return ok;
+}
+
 // Argmax of row[lo, hi) over the CTA (CH_THREADS threads); valid in every thread.
 template <bool VEC>
-__device__ ArgBest chunk_argmax(const float* __restrict__ row, int lo, int hi, ArgBest* red) {
+__device__ ArgBest chunk_argmax(const float* __restrict__ row, int lo, int hi, ArgBest* red,
+                                Ring& ring, bool& ok) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     ArgBest a{-INFINITY, NO_INDEX};
+    ok = true;
     if (VEC) {
-        const int nv = (hi - lo) >> 2;
-        const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-        constexpr int T = CH_THREADS;
-        int e = tid;
-        for (; e + 3 * T < nv; e += 4 * T) {
-            const float4 x0 = __ldg(r4 + e), x1 = __ldg(r4 + e + T);
-            const float4 x2 = __ldg(r4 + e + 2 * T), x3 = __ldg(r4 + e + 3 * T);
-            take4(a, x0, lo + 4 * e);
-            take4(a, x1, lo + 4 * (e + T));
-            take4(a, x2, lo + 4 * (e + 2 * T));
-            take4(a, x3, lo + 4 * (e + 3 * T));
-        }
-        for (; e < nv; e += T) take4(a, __ldg(r4 + e), lo + 4 * e);
-        for (int i = lo + 4 * nv + tid; i < hi; i += T) take(a, __ldg(row + i), i);
+        ok = stream_rows(row, nullptr, lo, hi, ring,
+                         [&](const float4& x, const float4&, int i) { take4(a, x, i); });
     } else {
         for (int i = lo + tid; i < hi; i += CH_THREADS) take(a, __ldg(row + i), i);
     }
@@ -429,11 +480,20 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     __shared__ int last;
     __shared__ int spar[64], stok[64], sam[64];
     __shared__ int sflag;
+    extern __shared__ __align__(1024) float ring_buf[];  // [STG][PIECE]
+    __shared__ uint64_t full[STG];
+    if (tid == 0) {
+        for (int k = 0; k < STG; ++k) mbar_init(&full[k], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Ring ring{ring_buf, full, 0u};
     const int per = chunk_len(p.V, ch);
     const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
-    const ArgBest a = chunk_argmax<VEC>(p.target + (int64_t)row * p.V, lo, hi, red);
+    bool ok;
+    const ArgBest a = chunk_argmax<VEC>(p.target + (int64_t)row * p.V, lo, hi, red, ring, ok);
     if (tid == 0) {
-        part[(int64_t)row * CH_MAX + c] = make_int2(__float_as_int(a.v), a.i);
+        part[(int64_t)row * CH_MAX + c] = make_int2(__float_as_int(a.v), ok ? a.i : TIMED_OUT);
         __threadfence();
         last = (atomicAdd(&row_tick[row], 1) == ch - 1);
     }
@@ -443,13 +503,16 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     __threadfence();
     if (tid < 32) {
         ArgBest x{-INFINITY, NO_INDEX};
+        bool late = false;
         for (int k = tid; k < ch; k += 32) {
             const int2 v = __ldcg(part + (int64_t)row * CH_MAX + k);
-            if (v.y != NO_INDEX && beats(__int_as_float(v.x), v.y, x.v, x.i)) {
+            late |= (v.y == TIMED_OUT);
+            if (v.y >= 0 && v.y != NO_INDEX && beats(__int_as_float(v.x), v.y, x.v, x.i)) {
                 x.v = __int_as_float(v.x);
                 x.i = v.y;
             }
         }
+        late = __any_sync(0xffffffffu, late);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
@@ -460,7 +523,7 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
             }
         }
         if (tid == 0) {
-            am[row] = (x.i == NO_INDEX) ? -1 : x.i;
+            am[row] = late ? TIMED_OUT : (x.i == NO_INDEX) ? -1 : x.i;
             row_tick[row] = 0;  // leave the workspace ready for the next call
             __threadfence();
             last = (atomicAdd(&seq_tick[b], 1) == N - 1);
@@ -484,6 +547,12 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
         }
     }
     __syncthreads();
+    if (sflag == TV_OK && tid < 32) {
+        bool late = false;
+        for (int k = tid; k < N; k += 32) late |= (sam[k] == TIMED_OUT);
+        if (__any_sync(0xffffffffu, late) && tid == 0) sflag = TV_ERR_TIMEOUT;
+    }
+    __syncthreads();
     if (sflag != TV_OK) {
         write_fail(p, b, sflag);
         return;
@@ -491,79 +560,108 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     walk_and_write(p, b, spar, stok, sam);
 }
 
-// Sum of integer weights over row a's chunk [lo, hi): weight(a - b) when b
-// is given (the residual), weight(a) otherwise; valid in thread 0.
+// Integer weights of row a over [lo, hi) (weight(a - b) when b is given, the
+// residual; weight(a) otherwise), streamed piece by piece: the sum of every
+// PIECE-element piece k goes to psum[k] (global, thread 0 writes it).  lo is a
+// multiple of PIECE.  Every thread of the CTA calls it; false on a timeout.
 template <bool VEC>
-__device__ uint64_t chunk_weight_sum(const float* a, const float* bq, int lo, int hi,
-                                     uint64_t* red) {
+__device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int hi, Ring& r,
+                                  uint64_t (*red)[CH_WARPS], uint64_t* psum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool resid = bq != nullptr;
-    uint64_t w = 0;
-    int i = lo;
-    if (VEC) {
-        const int nv = (hi - lo) >> 2;
-        const float4* a4 = reinterpret_cast<const float4*>(a + lo);
-        const float4* b4 = resid ? reinterpret_cast<const float4*>(bq + lo) : nullptr;
-        constexpr int T = CH_THREADS;
-        auto acc4 = [&](const float4& x, const float4& y) {
-            if (resid)
-                w += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
-                     weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
-            else
-                w += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
-        };
-        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        int e = tid;
-        for (; e + 3 * T < nv; e += 4 * T) {
-            const float4 x0 = __ldg(a4 + e), x1 = __ldg(a4 + e + T);
-            const float4 x2 = __ldg(a4 + e + 2 * T), x3 = __ldg(a4 + e + 3 * T);
-            const float4 y0 = resid ? __ldg(b4 + e) : z4, y1 = resid ? __ldg(b4 + e + T) : z4;
-            const float4 y2 = resid ? __ldg(b4 + e + 2 * T) : z4;
-            const float4 y3 = resid ? __ldg(b4 + e + 3 * T) : z4;
-            acc4(x0, y0);
-            acc4(x1, y1);
-            acc4(x2, y2);
-            acc4(x3, y3);
-        }
-        for (; e < nv; e += T) acc4(__ldg(a4 + e), resid ? __ldg(b4 + e) : z4);
-        i = lo + 4 * nv;
-    }
-    for (i += tid; i < hi; i += CH_THREADS) w += elem_weight(a, bq, i, resid);
+    const int np = (hi - lo + PIECE - 1) / PIECE;
+    if (!VEC) {
+        for (int k = 0; k < np; ++k) {
+            const int off = lo + k * PIECE, end = min(hi, off + PIECE);
+            uint64_t w = 0;
+            for (int i = off + tid; i < end; i += CH_THREADS) w += elem_weight(a, bq, i, resid);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
-    __syncthreads();  // red may still be read from an earlier call
-    if (lane == 0) red[warp] = w;
-    __syncthreads();
-    uint64_t tot = 0;
-    for (int k = 0; k < CH_WARPS; ++k) tot += red[k];
-    return tot;
+            for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+            if (lane == 0) red[0][warp] = w;
+            __syncthreads();
+            if (tid == 0) {
+                uint64_t t = 0;
+                for (int q = 0; q < CH_WARPS; ++q) t += red[0][q];
+                psum[(off) / PIECE] = t;
+            }
+            __syncthreads();
+        }
+        return true;
+    }
+    const int ops = resid ? 2 : 1;
+    const uint64_t pol = l2_policy_evict_first();
+    auto issue = [&](int k) {
+        const int st = (int)((r.pc + k) % STG);
+        const int off = lo + k * PIECE;
+        const uint32_t bytes = (uint32_t)min(PIECE, hi - off) * 4u;
+        mbar_arrive_expect_tx(&r.full[st], bytes * ops);
+        bulk_load(r.buf + (size_t)st * ops * PIECE, a + off, bytes, &r.full[st], pol);
+        if (resid) bulk_load(r.buf + (size_t)st * ops * PIECE + PIECE, bq + off, bytes, &r.full[st], pol);
+    };
+    if (tid == 0)
+        for (int k = 0; k < min(STG, np); ++k) issue(k);
+    bool ok = true;
+    int k = 0;
+    for (; k < np; ++k) {
+        const uint32_t g = r.pc + k;
+        const int st = (int)(g % STG);
+        const bool got = mbar_wait(&r.full[st], (g / STG) & 1u);
+        uint64_t w = 0;
+        if (got) {
+            const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
+            const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)st * ops * PIECE);
+            const float4* y4 = x4 + PIECE / 4;
+            for (int e = tid; e < n4; e += CH_THREADS) {
+                const float4 x = x4[e];
+                if (resid) {
+                    const float4 y = y4[e];
+                    w += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
+                         weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
+                } else {
+                    w += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) red[st][warp] = w;
+        ok = __syncthreads_and(got) != 0;  // every thread is done with stage st
+        if (!ok) break;
+        if (tid == 0) {
+            uint64_t t = 0;
+            for (int q = 0; q < CH_WARPS; ++q) t += red[st][q];
+            psum[(lo + k * PIECE) / PIECE] = t;
+            if (k + STG < np) issue(k + STG);
+        }
+    }
+    if (!ok && tid == 0) {
+        // let the copies still in flight land before the shared memory is released
+        for (int j = k + 1; j < min(np, k + STG); ++j) {
+            const uint32_t g = r.pc + j;
+            mbar_wait(&r.full[g % STG], (g / STG) & 1u);
+        }
+    }
+    r.pc += np;
+    return ok;
 }
 
-// Picks the chunk holding the draw: per-chunk sums v(k) (k < ch) come from
-// `get`; one full warp; returns the chunk (-1 when the total is zero) and the
-// remaining offset T inside it, in every lane.
+// Picks the index holding the draw among n values v(k) from `get` (a prefix
+// of k = 0.. in order); one full warp; returns the index (-1 when the total is
+// zero) and the offset T inside it, in every lane.
 template <typename Get>
-__device__ int pick_chunk(int ch, uint32_t x1, Get get, uint64_t& T, uint64_t& total) {
+__device__ int pick_index(int n, uint32_t x1, Get get, uint64_t& T) {
     const int lane = threadIdx.x & 31;
-    uint64_t v[CH_MAX / 32];
     uint64_t tot = 0;
-#pragma unroll
-    for (int q = 0; q < CH_MAX / 32; ++q) {
-        const int k = lane + 32 * q;
-        v[q] = (k < ch) ? get(k) : 0ull;
-        tot += v[q];
-    }
+    for (int k = lane; k < n; k += 32) tot += get(k);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-    total = tot;
     T = 0;
     if (tot == 0) return -1;
     const uint64_t hi = __umul64hi((uint64_t)x1, tot), lo = (uint64_t)x1 * tot;
     uint64_t t = (hi << 32) | (lo >> 32);
-    // chunk order k = 32 q + lane: scan each group of 32 in turn
-#pragma unroll
-    for (int q = 0; q < CH_MAX / 32; ++q) {
-        uint64_t x = v[q];
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const uint64_t v = (k0 + lane < n) ? get(k0 + lane) : 0ull;
+        uint64_t x = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const uint64_t y = __shfl_up_sync(0xffffffffu, x, off);
@@ -572,8 +670,8 @@ __device__ int pick_chunk(int ch, uint32_t x1, Get get, uint64_t& T, uint64_t& t
         const uint64_t grp = __shfl_sync(0xffffffffu, x, 31);
         if (t < grp) {
             const int l = __ffs(__ballot_sync(0xffffffffu, x > t)) - 1;
-            T = t - __shfl_sync(0xffffffffu, x - v[q], l);
-            return 32 * q + l;
+            T = t - __shfl_sync(0xffffffffu, x - v, l);
+            return k0 + l;
         }
         t -= grp;
     }
@@ -662,7 +760,7 @@ __device__ int chunk_find(const float* a, const float* bq, int lo, int hi, uint6
 }
 
 // Stochastic chain acceptance: CTA (b, c) takes chunk c of the row the token
-// is drawn from; ws: sums[b][CH_MAX] (weight sum of the chunk), seq_tick[b].
+// is drawn from; ws: sums[b][ceil(V / PIECE)] (weight sum of every piece), seq_tick[b].
 template <bool VEC>
 __global__ void __launch_bounds__(CH_THREADS)
 accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
@@ -673,8 +771,14 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
     __shared__ int spar[64], stok[64];
     __shared__ int sflag, skstar, last;
-    __shared__ uint64_t red[CH_WARPS];
-    __shared__ uint64_t tsum[FIND_TILES];
+    __shared__ uint64_t red[STG][CH_WARPS];
+    __shared__ uint64_t tsum[PIECE / 256];
+    extern __shared__ __align__(1024) float ring_buf[];  // [STG][2][PIECE]
+    __shared__ uint64_t full[STG];
+    if (tid == 0) {
+        for (int k = 0; k < STG; ++k) mbar_init(&full[k], 1);
+        fence_mbar_init();
+    }
     if (tid < N) {
         spar[tid] = p.parents[(int64_t)b * N + tid];
         stok[tid] = p.tokens[(int64_t)b * N + tid];
@@ -713,51 +817,60 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     const bool rejected = kstar <= K;
     const float* rowa = p.target + ((int64_t)b * N + (rejected ? kstar - 1 : K)) * p.V;
     const float* rowb = rejected ? p.draft + ((int64_t)b * N + kstar) * p.V : nullptr;
-    const int per = chunk_len(p.V, ch);
+    // chunk c: whole pieces [lo, hi); piece sums of sequence b at psum[b][*]
+    const int np_all = (p.V + PIECE - 1) / PIECE;
+    const int per = ((np_all + ch - 1) / ch) * PIECE;
+    uint64_t* psum = sums + (int64_t)b * np_all;
+    Ring ring{ring_buf, full, 0u};
     {
         const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
-        const uint64_t mine = chunk_weight_sum<VEC>(rowa, rowb, lo, hi, red);
+        const bool ok = piece_weight_sums<VEC>(rowa, rowb, lo, hi, ring, red, psum);
         if (tid == 0) {
-            sums[(int64_t)b * CH_MAX + c] = mine;
+            if (!ok) psum[lo / PIECE] = SUM_TIMED_OUT;
             __threadfence();
             last = (atomicAdd(&seq_tick[b], 1) == ch - 1);
         }
     }
     __syncthreads();
     if (!last) return;
-    // this CTA completed sequence b: pick the chunk holding the draw
+    // this CTA completed sequence b: pick the piece holding the draw
     __threadfence();
-    __shared__ int schunk, sresid;
-    __shared__ uint64_t sT, stot;
-    __shared__ uint64_t fsum[CH_MAX];
+    __shared__ int spiece, sresid, slate;
+    __shared__ uint64_t sT;
     const uint32_t x1 = draw(p, b, rejected ? kstar : K + 1).y;
     if (warp == 0) {
-        uint64_t T, tot;
-        const int cc = pick_chunk(ch, x1, [&](int k) { return __ldcg(sums + (int64_t)b * CH_MAX + k); },
-                                  T, tot);
+        bool late = false;
+        for (int k = lane; k < np_all; k += 32) late |= (__ldcg(psum + k) & SUM_TIMED_OUT) != 0;
+        late = __any_sync(0xffffffffu, late);
+        uint64_t T = 0;
+        const int pi = late ? -1 : pick_index(np_all, x1, [&](int k) { return __ldcg(psum + k); }, T);
         if (lane == 0) {
             seq_tick[b] = 0;  // leave the workspace ready for the next call
-            schunk = cc;
+            spiece = pi;
             sT = T;
-            stot = tot;
             sresid = rejected;
+            slate = late;
         }
     }
     __syncthreads();
-    if (rejected && stot == 0) {
+    if (slate) {
+        write_fail(p, b, TV_ERR_TIMEOUT);
+        return;
+    }
+    if (rejected && spiece < 0) {
         // the residual has no mass: draw from the target row itself (rare: this
-        // CTA sums every chunk of it)
-        for (int k = 0; k < ch; ++k) {
-            const int lo = min(p.V, k * per), hi = min(p.V, lo + per);
-            const uint64_t v = chunk_weight_sum<VEC>(rowa, nullptr, lo, hi, red);
-            if (tid == 0) fsum[k] = v;
+        // CTA sums every piece of it)
+        if (!piece_weight_sums<VEC>(rowa, nullptr, 0, p.V, ring, red, psum)) {
+            write_fail(p, b, TV_ERR_TIMEOUT);
+            return;
         }
-        __syncthreads();
+        __threadfence();
+        __syncthreads();  // thread 0's piece sums are visible to warp 0
         if (warp == 0) {
-            uint64_t T, tot;
-            const int cc = pick_chunk(ch, x1, [&](int k) { return fsum[k]; }, T, tot);
+            uint64_t T = 0;
+            const int pi = pick_index(np_all, x1, [&](int k) { return __ldcg(psum + k); }, T);
             if (lane == 0) {
-                schunk = cc;
+                spiece = pi;
                 sT = T;
                 sresid = 0;
             }
@@ -765,8 +878,8 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
         __syncthreads();
     }
     int token = -1;
-    if (schunk >= 0) {
-        const int lo = min(p.V, schunk * per), hi = min(p.V, lo + per);
+    if (spiece >= 0) {
+        const int lo = spiece * PIECE, hi = min(p.V, lo + PIECE);
         token = chunk_find(rowa, sresid ? rowb : nullptr, lo, hi, sT, tsum);
     }
     if (token < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
@@ -814,14 +927,23 @@ bool prefer_rowscan(int B, int N, int V) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Chunks per row: about four CTAs per multiprocessor over `rows` rows, at
-// least 1024 elements a chunk, and few enough that a chunk search fits.
-int chunks_for(int64_t rows, int V, int sms) {
-    int64_t ch = (4LL * sms + rows - 1) / rows;
-    ch = std::min<int64_t>(ch, std::max(1, V / 1024));
-    const int64_t need = ((int64_t)V + 256LL * FIND_TILES - 1) / (256LL * FIND_TILES);
-    ch = std::max<int64_t>(ch, need);
-    return (int)std::min<int64_t>(std::max<int64_t>(ch, 1), CH_MAX);
+// CTAs of `kern` resident on the whole device with `smem` dynamic bytes.
+template <typename K>
+int64_t resident_ctas(K kern, size_t smem, int sms) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, CH_THREADS, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    return (int64_t)std::max(n, 1) * sms;
+}
+
+// Chunks per row: as many as keep all `rows` x chunks CTAs resident at once
+// (one wave), with at least one piece per chunk.
+int chunks_for(int64_t rows, int V, int64_t resident) {
+    int64_t ch = std::max<int64_t>(1, resident / rows);
+    ch = std::min<int64_t>(ch, std::max(1, (V + PIECE - 1) / PIECE));
+    return (int)std::min<int64_t>(ch, CH_MAX);
 }
 
 struct RowsWs {
@@ -837,7 +959,21 @@ RowsWs rows_ws(int B, int N) {
     w.total = w.seq_tick + align256((size_t)B * 4);
     return w;
 }
-size_t stoch_ws_sums(int B) { return align256((size_t)B * CH_MAX * 8); }
+constexpr size_t ROWS_SMEM = (size_t)STG * PIECE * 4 + 1024;       // ring, one operand
+constexpr size_t STOCH_SMEM = (size_t)STG * 2 * PIECE * 4 + 1024;  // ring, two operands
+
+bool stoch_attr() {
+    static int state = -1;
+    if (state < 0)
+        state = (cudaFuncSetAttribute(accept_stochastic_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)STOCH_SMEM) == cudaSuccess)
+                    ? 1
+                    : 0;
+    return state == 1;
+}
+
+size_t stoch_ws_sums(int B, int V) { return align256((size_t)B * ((V + PIECE - 1) / PIECE) * 8); }
 
 }  // namespace
 
@@ -845,7 +981,7 @@ size_t accept_workspace(tv_accept_mode mode, int B, int N, int V) {
     if (B <= 0) return 0;
     if (mode == TV_ACCEPT_GREEDY)
         return prefer_rowscan(B, N, V) ? rows_ws(B, N).total : 0;
-    return stoch_ws_sums(B) + align256((size_t)B * 4);
+    return stoch_ws_sums(B, V) + align256((size_t)B * 4);
 }
 
 tv_status launch_accept(const AcceptArgs& a) {
@@ -875,14 +1011,16 @@ tv_status launch_accept(const AcceptArgs& a) {
     cudaError_t e;
     if (a.mode == TV_ACCEPT_GREEDY && need > 0) {
         const int64_t R = (int64_t)a.B * a.N;
-        const int ch = chunks_for(R, a.V, sms);
+        static int64_t cap = -1;
+        if (cap < 0) cap = resident_ctas(accept_rows_kernel<true>, ROWS_SMEM, sms);
+        const int ch = chunks_for(R, a.V, cap);
         if (R * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
         const RowsWs w = rows_ws(a.B, a.N);
         int2* part = reinterpret_cast<int2*>(ws + w.part);
         int32_t* am = reinterpret_cast<int32_t*>(ws + w.am);
         int32_t* rt = reinterpret_cast<int32_t*>(ws + w.row_tick);
         int32_t* st = reinterpret_cast<int32_t*>(ws + w.seq_tick);
-        LaunchCfg lc(dim3((unsigned)(R * ch)), dim3(CH_THREADS), 0, a.stream);
+        LaunchCfg lc(dim3((unsigned)(R * ch)), dim3(CH_THREADS), vec ? ROWS_SMEM : 0, a.stream);
         e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<true>, p, ch, part, am, rt, st)
                 : cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<false>, p, ch, part, am, rt, st);
     } else if (a.mode == TV_ACCEPT_GREEDY) {
@@ -895,11 +1033,14 @@ tv_status launch_accept(const AcceptArgs& a) {
         e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<true>, p)
                 : cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<false>, p);
     } else {
-        const int ch = chunks_for(a.B, a.V, sms);
+        static int64_t cap = -1;
+        if (!stoch_attr()) return TV_ERR_CUDA;
+        if (cap < 0) cap = resident_ctas(accept_stochastic_kernel<true>, STOCH_SMEM, sms);
+        const int ch = chunks_for(a.B, a.V, cap);
         if ((int64_t)a.B * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
         uint64_t* sums = reinterpret_cast<uint64_t*>(ws);
-        int32_t* st = reinterpret_cast<int32_t*>(ws + stoch_ws_sums(a.B));
-        LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), 0, a.stream);
+        int32_t* st = reinterpret_cast<int32_t*>(ws + stoch_ws_sums(a.B, a.V));
+        LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), vec ? STOCH_SMEM : 0, a.stream);
         e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<true>, p, ch, sums, st)
                 : cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<false>, p, ch, sums, st);
     }
