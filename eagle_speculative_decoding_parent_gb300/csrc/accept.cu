@@ -10,9 +10,9 @@
 //                 token.  Rows read ~ accepted depth + 1.
 //   greedy rows   (small batches) every row's argmax in parallel: each row is
 //                 cut into chunks, one CTA per chunk; partial results go to the
-//                 workspace, the CTA that completes a row (arrival counter)
-//                 reduces it, and the CTA that completes a sequence walks its
-//                 tree.  Reads every row once, without the walk's latency.
+//                 workspace and the CTA that completes a sequence (arrival
+//                 counter) reduces them and walks its tree.  Reads every row
+//                 once, without the walk's latency.
 //   stochastic    the accept tests touch two scalars per draft (all evaluated at
 //                 once, the first failure wins); only the row(s) the emitted
 //                 token is drawn from are read, cut into chunks, one CTA per
@@ -35,8 +35,6 @@ namespace tv {
 
 namespace {
 
-constexpr int ACC_THREADS = 512;
-constexpr int ACC_WARPS = ACC_THREADS / 32;
 constexpr int NO_INDEX = 0x7fffffff;
 constexpr int TIMED_OUT = -2;      // a row argmax whose data did not arrive in time
 constexpr uint64_t SUM_TIMED_OUT = 1ull << 63;  // a chunk sum whose data did not arrive
@@ -121,64 +119,6 @@ __device__ __forceinline__ uint64_t elem_weight(const float* a, const float* bq,
     return resid ? weight(__fsub_rn(__ldg(a + t), __ldg(bq + t))) : weight(__ldg(a + t));
 }
 
-struct Slice {
-    int lo, hi;      // this CTA's vocabulary range
-    int seg;         // elements per warp segment (multiple of 4)
-};
-
-__device__ __forceinline__ Slice make_slice(int V, int C, int rank) {
-    int per = (V + C - 1) / C;
-    per = (per + 3) & ~3;
-    Slice s;
-    s.lo = min(V, rank * per);
-    s.hi = min(V, s.lo + per);
-    int seg = (s.hi - s.lo + ACC_WARPS - 1) / ACC_WARPS;
-    s.seg = (seg + 3) & ~3;
-    return s;
-}
-
-// Block-wide argmax of row[lo, hi); result valid in every thread.
-template <bool VEC>
-__device__ ArgBest block_argmax(const float* __restrict__ row, int lo, int hi, ArgBest* red) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    ArgBest a{-INFINITY, NO_INDEX};
-    if (VEC) {
-        const int nv = (hi - lo) >> 2;
-        const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-        constexpr int T = ACC_THREADS;
-        int e = tid;
-        // four independent 16-byte loads in flight before any compare
-        for (; e + 3 * T < nv; e += 4 * T) {
-            const float4 x0 = __ldg(r4 + e), x1 = __ldg(r4 + e + T);
-            const float4 x2 = __ldg(r4 + e + 2 * T), x3 = __ldg(r4 + e + 3 * T);
-            take4(a, x0, lo + 4 * e);
-            take4(a, x1, lo + 4 * (e + T));
-            take4(a, x2, lo + 4 * (e + 2 * T));
-            take4(a, x3, lo + 4 * (e + 3 * T));
-        }
-        for (; e < nv; e += T) take4(a, __ldg(r4 + e), lo + 4 * e);
-        for (int i = lo + 4 * nv + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
-    } else {
-        for (int i = lo + tid; i < hi; i += ACC_THREADS) take(a, __ldg(row + i), i);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, a.v, off);
-        const int j = __shfl_xor_sync(0xffffffffu, a.i, off);
-        if (beats(w, j, a.v, a.i)) {
-            a.v = w;
-            a.i = j;
-        }
-    }
-    __syncthreads();
-    if (lane == 0) red[warp] = a;
-    __syncthreads();
-    ArgBest r = red[0];
-    for (int w = 1; w < ACC_WARPS; ++w)
-        if (beats(red[w].v, red[w].i, r.v, r.i)) r = red[w];
-    return r;
-}
-
 __device__ void write_fail(const AccParams& p, int b, int st) {
     for (int j = threadIdx.x; j < p.max_path; j += blockDim.x) {
         p.path[(int64_t)b * p.max_path + j] = (j == 0) ? 0 : -1;
@@ -235,102 +175,15 @@ __device__ int check_inputs(const int* spar, const int* stok, int N, int V, bool
         chain_bad |= (i > 0 && pa != i - 1);
         tok_bad |= (i > 0 && (stok[i] < 0 || stok[i] >= V));
     }
-    if (__any_sync(0xffffffffu, tree_bad)) return TV_ERR_BAD_TREE;
-    if (chain && __any_sync(0xffffffffu, chain_bad)) return TV_ERR_UNSUPPORTED;
-    if (__any_sync(0xffffffffu, tok_bad)) return TV_ERR_OUT_OF_RANGE;
+    const bool any_tree = __any_sync(0xffffffffu, tree_bad);
+    const bool any_chain = __any_sync(0xffffffffu, chain_bad);
+    const bool any_tok = __any_sync(0xffffffffu, tok_bad);
+    if (any_tree) return TV_ERR_BAD_TREE;
+    if (chain && any_chain) return TV_ERR_UNSUPPORTED;
+    if (any_tok) return TV_ERR_OUT_OF_RANGE;
     return TV_OK;
 }
 
-template <bool VEC>
-__global__ void __launch_bounds__(ACC_THREADS)
-accept_greedy_kernel(AccParams p) {
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
-    const int rank = (int)cluster.block_rank();
-    pdl_launch_dependents();
-    pdl_wait();
-    const int b = blockIdx.x / C;
-    __shared__ int spar[64], stok[64], sam[64];
-    __shared__ ArgBest exch[2][64];
-    __shared__ ArgBest red[ACC_WARPS];
-    __shared__ int sflag;
-    const int tid = threadIdx.x, N = p.N;
-    if (tid < N) {
-        spar[tid] = p.parents[(int64_t)b * N + tid];
-        stok[tid] = p.tokens[(int64_t)b * N + tid];
-        sam[tid] = -1;
-    }
-    __syncthreads();
-    if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V, false);
-        if (tid == 0) sflag = f;
-    }
-    __syncthreads();
-    if (sflag != TV_OK) {
-        if (rank == 0) write_fail(p, b, sflag);
-        return;  // uniform across the cluster: no cluster barrier has been issued
-    }
-    const Slice sl = make_slice(p.V, C, rank);
-    uint64_t frontier = 1ull;  // node 0
-    int par = 0, chosen = 0;
-    // each level is one depth deeper, so the walk ends within N levels
-    for (int level = 0; level < N; ++level) {
-        // local argmax of each frontier row
-        for (uint64_t f = frontier; f; f &= f - 1) {
-            const int u = __ffsll((long long)f) - 1;
-            const float* row = p.target + ((int64_t)b * N + u) * p.V;
-            const ArgBest a = block_argmax<VEC>(row, sl.lo, sl.hi, red);
-            if (tid == 0) exch[par][u] = a;
-        }
-        cluster.sync();
-        // combine across the cluster: warp w takes frontier nodes w, w+16, ...;
-        // lane r reads rank r's candidate, then a warp argmax
-        {
-            const int warp = tid >> 5, lane = tid & 31;
-            int idx = 0;
-            for (uint64_t f = frontier; f; f &= f - 1, ++idx) {
-                if (idx % ACC_WARPS != warp) continue;
-                const int u = __ffsll((long long)f) - 1;
-                ArgBest x{-INFINITY, NO_INDEX};
-                if (lane < C) x = *cluster.map_shared_rank(&exch[par][u], lane);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
-                    const int j = __shfl_xor_sync(0xffffffffu, x.i, off);
-                    if (beats(w, j, x.v, x.i)) {
-                        x.v = w;
-                        x.i = j;
-                    }
-                }
-                if (lane == 0) sam[u] = (x.i == NO_INDEX) ? -1 : x.i;
-            }
-        }
-        __syncthreads();
-        // next frontier: children whose token equals their (frontier) parent's argmax
-        __shared__ unsigned long long snext;
-        if (tid == 0) snext = 0ull;
-        __syncthreads();
-        if (tid >= 1 && tid < N) {
-            const int pc = spar[tid];
-            if (((frontier >> pc) & 1ull) && sam[pc] >= 0 && stok[tid] == sam[pc])
-                atomicOr(&snext, 1ull << tid);
-        }
-        __syncthreads();
-        const uint64_t next = snext;
-        if (next == 0) {
-            chosen = __ffsll((long long)frontier) - 1;
-            break;
-        }
-        frontier = next;
-        par ^= 1;
-        __syncthreads();  // snext is reset at the next level
-    }
-    cluster.sync();  // no CTA leaves while others may still read its exchange slots
-    if (rank == 0) {
-        if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
-        else write_path(p, b, spar, stok, chosen, sam[chosen]);
-    }
-}
 
 constexpr int CH_THREADS = 256;            // CTA size of the chunked kernels
 constexpr int CH_WARPS = CH_THREADS / 32;
@@ -348,9 +201,10 @@ constexpr int PIECE = 2048;
 constexpr int STG = 4;
 
 struct Ring {
-    float* buf;        // [STG][ops][PIECE]
-    uint64_t* full;    // [STG]
+    float* buf;        // [stg][ops][PIECE]
+    uint64_t* full;    // [stg]
     uint32_t pc;       // pieces this CTA has consumed (ring position and phase)
+    int stg;           // pieces in flight
 };
 
 // Calls f(x, y, i) for x = a[i..i+3] and y = b[i..i+3] (zeros without b), for
@@ -365,7 +219,7 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
     const int np = (hi - lo + PIECE - 1) / PIECE;
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int k) {
-        const int s = (int)((r.pc + k) % STG);
+        const int s = (int)((r.pc + k) % r.stg);
         const int off = lo + k * PIECE;
         const uint32_t bytes = (uint32_t)min(PIECE, hi - off) * 4u;
         mbar_arrive_expect_tx(&r.full[s], bytes * ops);
@@ -373,14 +227,39 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
         if (b) bulk_load(r.buf + (size_t)s * ops * PIECE + PIECE, b + off, bytes, &r.full[s], pol);
     };
     if (tid == 0)
-        for (int k = 0; k < min(STG, np); ++k) issue(k);
+        for (int k = 0; k < min(r.stg, np); ++k) issue(k);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (np <= r.stg) {
+        // everything is in flight at once: consume the pieces as they land, one
+        // barrier at the end
+        bool got = true;
+        for (int k = 0; k < np; ++k) {
+            const uint32_t g = r.pc + k;
+            const int s = (int)(g % r.stg);
+            got = got && mbar_wait(&r.full[s], (g / r.stg) & 1u);
+            if (got) {
+                const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
+                const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)s * ops * PIECE);
+                const float4* y4 = x4 + PIECE / 4;
+                for (int e = tid; e < n4; e += blockDim.x) f(x4[e], b ? y4[e] : z4, off + 4 * e);
+            }
+        }
+        const bool ok = __syncthreads_and(got) != 0;
+        if (!ok && tid == 0) {
+            for (int k = 0; k < np; ++k) {
+                const uint32_t g = r.pc + k;
+                mbar_wait(&r.full[g % r.stg], (g / r.stg) & 1u);
+            }
+        }
+        r.pc += np;
+        return ok;
+    }
     bool ok = true;
     int k = 0;
     for (; k < np; ++k) {
         const uint32_t g = r.pc + k;
-        const int s = (int)(g % STG);
-        const bool got = mbar_wait(&r.full[s], (g / STG) & 1u);
+        const int s = (int)(g % r.stg);
+        const bool got = mbar_wait(&r.full[s], (g / r.stg) & 1u);
         if (got) {
             const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
             const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)s * ops * PIECE);
@@ -389,17 +268,53 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
         }
         ok = __syncthreads_and(got) != 0;  // every thread is done with stage s
         if (!ok) break;
-        if (tid == 0 && k + STG < np) issue(k + STG);
+        if (tid == 0 && k + r.stg < np) issue(k + r.stg);
     }
     if (!ok && tid == 0) {
         // let the copies still in flight land before the shared memory is released
-        for (int j = k + 1; j < min(np, k + STG); ++j) {
+        for (int j = k + 1; j < min(np, k + r.stg); ++j) {
             const uint32_t g = r.pc + j;
-            mbar_wait(&r.full[g % STG], (g / STG) & 1u);
+            mbar_wait(&r.full[g % r.stg], (g / r.stg) & 1u);
         }
     }
     r.pc += np;
     return ok;
+}
+
+// Argmax of row[lo, hi) with every thread's loads in flight at once (twelve
+// 16-byte loads per thread per round): for short, latency-bound slices.
+// lo and hi - lo are multiples of 4 and the row 16-byte aligned.
+__device__ ArgBest slice_argmax_ldg(const float* __restrict__ row, int lo, int hi, ArgBest* red) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    ArgBest a{-INFINITY, NO_INDEX};
+    const int n4 = (hi - lo) >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+    constexpr int T = CH_THREADS, U = 12;
+    for (int e0 = 0; e0 < n4; e0 += U * T) {
+        float4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * T + tid;
+            x[u] = (e < n4) ? __ldg(r4 + e) : make_float4(NAN, NAN, NAN, NAN);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) take4(a, x[u], lo + 4 * (e0 + u * T + tid));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, a.v, off);
+        const int j = __shfl_xor_sync(0xffffffffu, a.i, off);
+        if (beats(w, j, a.v, a.i)) {
+            a.v = w;
+            a.i = j;
+        }
+    }
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    ArgBest r = red[0];
+    for (int w = 1; w < CH_WARPS; ++w)
+        if (beats(red[w].v, red[w].i, r.v, r.i)) r = red[w];
+    return r;
 }
 
 // Argmax of row[lo, hi) over the CTA (CH_THREADS threads); valid in every thread.
@@ -464,30 +379,36 @@ __device__ void walk_and_write(const AccParams& p, int b, const int* spar, const
 }
 
 // Greedy acceptance, every row in parallel: CTA (row, c) takes chunk c of the
-// row; ws: part[row][CH_MAX] (value bits, index), am[row], row_tick[row],
-// seq_tick[b].
+// row; ws: part[row][CH_MAX] (value bits, index of the chunk's argmax),
+// seq_tick[b] (arrivals of the sequence's N x ch CTAs).
 template <bool VEC>
 __global__ void __launch_bounds__(CH_THREADS)
-accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __restrict__ am,
-                   int32_t* __restrict__ row_tick, int32_t* __restrict__ seq_tick) {
+accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __restrict__ seq_tick) {
     pdl_launch_dependents();
     pdl_wait();
     const int N = p.N;
     const int row = blockIdx.x / ch, c = blockIdx.x % ch;
     const int b = row / N;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ ArgBest red[CH_WARPS];
     __shared__ int last;
     __shared__ int spar[64], stok[64], sam[64];
     __shared__ int sflag;
     extern __shared__ __align__(1024) float ring_buf[];  // [STG][PIECE]
     __shared__ uint64_t full[STG];
+    // the tree is only needed by the CTA that completes the sequence; its loads
+    // are issued now so they are in flight while the row streams
+    int par_v = 0, tok_v = 0;
+    if (tid < N) {
+        par_v = p.parents[(int64_t)b * N + tid];
+        tok_v = p.tokens[(int64_t)b * N + tid];
+    }
     if (tid == 0) {
         for (int k = 0; k < STG; ++k) mbar_init(&full[k], 1);
         fence_mbar_init();
     }
     __syncthreads();
-    Ring ring{ring_buf, full, 0u};
+    Ring ring{ring_buf, full, 0u, STG};
     const int per = chunk_len(p.V, ch);
     const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
     bool ok;
@@ -495,24 +416,37 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     if (tid == 0) {
         part[(int64_t)row * CH_MAX + c] = make_int2(__float_as_int(a.v), ok ? a.i : TIMED_OUT);
         __threadfence();
-        last = (atomicAdd(&row_tick[row], 1) == ch - 1);
+        last = (atomicAdd(&seq_tick[b], 1) == N * ch - 1);
     }
     __syncthreads();
     if (!last) return;
-    // this CTA completed the row: reduce its chunks
+    // this CTA completed sequence b: reduce every row's chunks (warp w takes
+    // rows w, w + 8, ...), then walk the tree
     __threadfence();
-    if (tid < 32) {
+    if (tid < N) {
+        spar[tid] = par_v;
+        stok[tid] = tok_v;
+    }
+    // lane k holds chunk k (ch <= 32) of each of the warp's rows; all loads are
+    // issued before any is used
+    int2 pv[64 / CH_WARPS];
+#pragma unroll
+    for (int q = 0; q < 64 / CH_WARPS; ++q) {
+        const int r = warp + q * CH_WARPS;
+        pv[q] = (r < N && lane < ch) ? __ldcg(part + ((int64_t)b * N + r) * CH_MAX + lane)
+                                     : make_int2(0, NO_INDEX);
+    }
+#pragma unroll
+    for (int q = 0; q < 64 / CH_WARPS; ++q) {
+        const int r = warp + q * CH_WARPS;
+        if (r >= N) break;
+        const int2 v = pv[q];
         ArgBest x{-INFINITY, NO_INDEX};
-        bool late = false;
-        for (int k = tid; k < ch; k += 32) {
-            const int2 v = __ldcg(part + (int64_t)row * CH_MAX + k);
-            late |= (v.y == TIMED_OUT);
-            if (v.y >= 0 && v.y != NO_INDEX && beats(__int_as_float(v.x), v.y, x.v, x.i)) {
-                x.v = __int_as_float(v.x);
-                x.i = v.y;
-            }
+        if (v.y >= 0 && v.y != NO_INDEX) {
+            x.v = __int_as_float(v.x);
+            x.i = v.y;
         }
-        late = __any_sync(0xffffffffu, late);
+        const bool late = __any_sync(0xffffffffu, v.y == TIMED_OUT);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
@@ -522,35 +456,19 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
                 x.i = j;
             }
         }
-        if (tid == 0) {
-            am[row] = late ? TIMED_OUT : (x.i == NO_INDEX) ? -1 : x.i;
-            row_tick[row] = 0;  // leave the workspace ready for the next call
-            __threadfence();
-            last = (atomicAdd(&seq_tick[b], 1) == N - 1);
-        }
-    }
-    __syncthreads();
-    if (!last) return;
-    // this CTA completed sequence b: walk its tree
-    __threadfence();
-    if (tid < N) {
-        spar[tid] = p.parents[(int64_t)b * N + tid];
-        stok[tid] = p.tokens[(int64_t)b * N + tid];
-        sam[tid] = __ldcg(am + (int64_t)b * N + tid);
+        if (lane == 0) sam[r] = late ? TIMED_OUT : (x.i == NO_INDEX) ? -1 : x.i;
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V, false);
-        if (tid == 0) {
-            seq_tick[b] = 0;
-            sflag = f;
-        }
-    }
-    __syncthreads();
-    if (sflag == TV_OK && tid < 32) {
+        int f = check_inputs(spar, stok, N, p.V, false);
         bool late = false;
         for (int k = tid; k < N; k += 32) late |= (sam[k] == TIMED_OUT);
-        if (__any_sync(0xffffffffu, late) && tid == 0) sflag = TV_ERR_TIMEOUT;
+        const bool any_late = __any_sync(0xffffffffu, late);
+        if (f == TV_OK && any_late) f = TV_ERR_TIMEOUT;
+        if (tid == 0) {
+            seq_tick[b] = 0;  // leave the workspace ready for the next call
+            sflag = f;
+        }
     }
     __syncthreads();
     if (sflag != TV_OK) {
@@ -558,6 +476,140 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
         return;
     }
     walk_and_write(p, b, spar, stok, sam);
+}
+
+// Greedy acceptance, level by level: one cluster of C CTAs per sequence, CTA
+// `rank` owns vocabulary slice [rank * per, ...).  Each level streams the
+// slice of every frontier row, exchanges the per-CTA argmax through
+// distributed shared memory, and keeps the children whose token equals their
+// parent's argmax.  All CTAs see the same exchanged values, so they take the
+// same decisions and reach every cluster barrier.
+template <bool VEC>
+__global__ void __launch_bounds__(CH_THREADS)
+accept_walk_kernel(AccParams p) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x / C;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
+    __shared__ int spar[64], stok[64], sam[64];
+    __shared__ ArgBest exch[2][64];
+    __shared__ ArgBest red[CH_WARPS];
+    __shared__ int sflag;
+    __shared__ unsigned long long snext;
+    if (tid < N) {
+        spar[tid] = p.parents[(int64_t)b * N + tid];
+        stok[tid] = p.tokens[(int64_t)b * N + tid];
+        sam[tid] = -1;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int f = check_inputs(spar, stok, N, p.V, false);
+        if (tid == 0) sflag = f;
+    }
+    __syncthreads();
+    if (sflag != TV_OK) {
+        if (rank == 0) write_fail(p, b, sflag);
+        return;  // uniform across the cluster: no cluster barrier has been issued
+    }
+    const int per = chunk_len(p.V, C);
+    const int lo = min(p.V, rank * per), hi = min(p.V, lo + per);
+    uint64_t frontier = 1ull;  // node 0
+    int par = 0, chosen = 0, status = TV_OK;
+    // each level is one depth deeper, so the walk ends within N levels
+    for (int level = 0; level < N; ++level) {
+        for (uint64_t f = frontier; f; f &= f - 1) {
+            const int u = __ffsll((long long)f) - 1;
+            const float* row = p.target + ((int64_t)b * N + u) * p.V;
+            ArgBest a;
+            if (VEC) {
+                a = slice_argmax_ldg(row, lo, hi, red);
+            } else {
+                a = ArgBest{-INFINITY, NO_INDEX};
+                for (int i = lo + tid; i < hi; i += CH_THREADS) take(a, __ldg(row + i), i);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float w = __shfl_xor_sync(0xffffffffu, a.v, off);
+                    const int j = __shfl_xor_sync(0xffffffffu, a.i, off);
+                    if (beats(w, j, a.v, a.i)) {
+                        a.v = w;
+                        a.i = j;
+                    }
+                }
+                if (lane == 0) red[warp] = a;
+                __syncthreads();
+                a = red[0];
+                for (int w = 1; w < CH_WARPS; ++w)
+                    if (beats(red[w].v, red[w].i, a.v, a.i)) a = red[w];
+            }
+            if (tid == 0) exch[par][u] = a;
+            __syncthreads();  // red is reused by the next row
+        }
+        cluster.sync();
+        // combine across the cluster: warp w takes frontier nodes w, w + 8, ...;
+        // lane r reads rank r's candidate, then a warp argmax
+        {
+            int idx = 0;
+            for (uint64_t f = frontier; f; f &= f - 1, ++idx) {
+                if (idx % CH_WARPS != warp) continue;
+                const int u = __ffsll((long long)f) - 1;
+                ArgBest x{-INFINITY, NO_INDEX};
+                if (lane < C) x = *cluster.map_shared_rank(&exch[par][u], lane);
+                const bool late = __any_sync(0xffffffffu, x.i == TIMED_OUT);
+                if (x.i == TIMED_OUT) x.i = NO_INDEX;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float w = __shfl_xor_sync(0xffffffffu, x.v, off);
+                    const int j = __shfl_xor_sync(0xffffffffu, x.i, off);
+                    if (beats(w, j, x.v, x.i)) {
+                        x.v = w;
+                        x.i = j;
+                    }
+                }
+                if (lane == 0) sam[u] = late ? TIMED_OUT : (x.i == NO_INDEX) ? -1 : x.i;
+            }
+        }
+        __syncthreads();
+        // next frontier: children whose token equals their (frontier) parent's argmax
+        if (warp == 0) {
+            uint64_t next = 0;
+            bool late = false;
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                const int c = c0 + lane;
+                bool hit = false;
+                if (c < N) {
+                    late |= ((frontier >> c) & 1ull) && sam[c] == TIMED_OUT;
+                    if (c >= 1) {
+                        const int pc = spar[c];
+                        hit = ((frontier >> pc) & 1ull) && sam[pc] >= 0 && stok[c] == sam[pc];
+                    }
+                }
+                next |= (uint64_t)__ballot_sync(0xffffffffu, hit) << c0;
+            }
+            const bool any_late = __any_sync(0xffffffffu, late);  // every lane votes
+            if (lane == 0) snext = any_late ? ~0ull : next;
+        } 
+        __syncthreads();
+        const uint64_t next = snext;
+        if (next == ~0ull) {
+            status = TV_ERR_TIMEOUT;
+            break;
+        }
+        if (next == 0) {
+            chosen = __ffsll((long long)frontier) - 1;
+            break;
+        }
+        frontier = next;
+        par ^= 1;
+    }
+    cluster.sync();  // no CTA leaves while others may still read its exchange slots
+    if (rank == 0) {
+        if (status != TV_OK) write_fail(p, b, status);
+        else if (sam[chosen] < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+        else write_path(p, b, spar, stok, chosen, sam[chosen]);
+    }
 }
 
 // Integer weights of row a over [lo, hi) (weight(a - b) when b is given, the
@@ -591,7 +643,7 @@ __device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int h
     const int ops = resid ? 2 : 1;
     const uint64_t pol = l2_policy_evict_first();
     auto issue = [&](int k) {
-        const int st = (int)((r.pc + k) % STG);
+        const int st = (int)((r.pc + k) % r.stg);
         const int off = lo + k * PIECE;
         const uint32_t bytes = (uint32_t)min(PIECE, hi - off) * 4u;
         mbar_arrive_expect_tx(&r.full[st], bytes * ops);
@@ -599,13 +651,13 @@ __device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int h
         if (resid) bulk_load(r.buf + (size_t)st * ops * PIECE + PIECE, bq + off, bytes, &r.full[st], pol);
     };
     if (tid == 0)
-        for (int k = 0; k < min(STG, np); ++k) issue(k);
+        for (int k = 0; k < min(r.stg, np); ++k) issue(k);
     bool ok = true;
     int k = 0;
     for (; k < np; ++k) {
         const uint32_t g = r.pc + k;
-        const int st = (int)(g % STG);
-        const bool got = mbar_wait(&r.full[st], (g / STG) & 1u);
+        const int st = (int)(g % r.stg);
+        const bool got = mbar_wait(&r.full[st], (g / r.stg) & 1u);
         uint64_t w = 0;
         if (got) {
             const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
@@ -631,14 +683,14 @@ __device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int h
             uint64_t t = 0;
             for (int q = 0; q < CH_WARPS; ++q) t += red[st][q];
             psum[(lo + k * PIECE) / PIECE] = t;
-            if (k + STG < np) issue(k + STG);
+            if (k + r.stg < np) issue(k + r.stg);
         }
     }
     if (!ok && tid == 0) {
         // let the copies still in flight land before the shared memory is released
-        for (int j = k + 1; j < min(np, k + STG); ++j) {
+        for (int j = k + 1; j < min(np, k + r.stg); ++j) {
             const uint32_t g = r.pc + j;
-            mbar_wait(&r.full[g % STG], (g / STG) & 1u);
+            mbar_wait(&r.full[g % r.stg], (g / r.stg) & 1u);
         }
     }
     r.pc += np;
@@ -821,7 +873,7 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     const int np_all = (p.V + PIECE - 1) / PIECE;
     const int per = ((np_all + ch - 1) / ch) * PIECE;
     uint64_t* psum = sums + (int64_t)b * np_all;
-    Ring ring{ring_buf, full, 0u};
+    Ring ring{ring_buf, full, 0u, STG};
     {
         const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
         const bool ok = piece_weight_sums<VEC>(rowa, rowb, lo, hi, ring, red, psum);
@@ -886,36 +938,6 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     else write_path(p, b, spar, stok, rejected ? kstar - 1 : K, token);
 }
 
-// Allows 16-CTA clusters for the walk kernels when the device supports it.
-bool enable_large_clusters() {
-    static int state = -1;
-    if (state < 0) {
-        state = 0;
-        bool ok = cudaFuncSetAttribute(accept_greedy_kernel<true>,
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        ok = ok && cudaFuncSetAttribute(accept_greedy_kernel<false>,
-                                        cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
-        if (ok) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(16);
-            cfg.blockDim = dim3(ACC_THREADS);
-            cudaLaunchAttribute at;
-            at.id = cudaLaunchAttributeClusterDimension;
-            at.val.clusterDim.x = 16;
-            at.val.clusterDim.y = 1;
-            at.val.clusterDim.z = 1;
-            cfg.attrs = &at;
-            cfg.numAttrs = 1;
-            int n = 0;
-            ok = cudaOccupancyMaxActiveClusters(&n, accept_greedy_kernel<true>, &cfg) == cudaSuccess &&
-                 n > 0;
-        }
-        cudaGetLastError();
-        state = ok ? 1 : 0;
-    }
-    return state == 1;
-}
-
 // The row scan pays for every row once at full bandwidth; the walk pays a few
 // microseconds of latency per tree level (at most 8 levels assumed).
 bool prefer_rowscan(int B, int N, int V) {
@@ -947,15 +969,13 @@ int chunks_for(int64_t rows, int V, int64_t resident) {
 }
 
 struct RowsWs {
-    size_t part, am, row_tick, seq_tick, total;
+    size_t part, seq_tick, total;
 };
 RowsWs rows_ws(int B, int N) {
     const size_t R = (size_t)B * N;
     RowsWs w;
     w.part = 0;
-    w.am = w.part + align256(R * CH_MAX * 8);
-    w.row_tick = w.am + align256(R * 4);
-    w.seq_tick = w.row_tick + align256(R * 4);
+    w.seq_tick = w.part + align256(R * CH_MAX * 8);
     w.total = w.seq_tick + align256((size_t)B * 4);
     return w;
 }
@@ -971,6 +991,43 @@ bool stoch_attr() {
                     ? 1
                     : 0;
     return state == 1;
+}
+
+// Clusters of cs walk CTAs that can be resident at once (0: cannot launch).
+int walk_clusters(int cs) {
+    static int cache[17] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    if (cs < 1 || cs > 16) return 0;
+    if (cache[cs] >= 0) return cache[cs];
+    int n = 0;
+    bool ok = true;
+    if (cs > 8)
+        ok = cudaFuncSetAttribute(accept_walk_kernel<true>,
+                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+             cudaFuncSetAttribute(accept_walk_kernel<false>,
+                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (ok) {
+        LaunchCfg lc(dim3(cs), dim3(CH_THREADS), 0, nullptr, (unsigned)cs);
+        lc.cfg.numAttrs = 1;  // the cluster shape only
+        if (cudaOccupancyMaxActiveClusters(&n, accept_walk_kernel<true>, &lc.cfg) != cudaSuccess)
+            n = 0;
+    }
+    cudaGetLastError();
+    cache[cs] = n;
+    return n;
+}
+
+// Largest cluster (at most 16 CTAs, at least PIECE vocabulary entries per CTA)
+// whose B clusters are resident at once; else the largest that launches.
+int walk_cluster_size(int B, int V) {
+    int fallback = 0;
+    for (int cs = 16; cs >= 1; cs >>= 1) {
+        if (cs > 1 && (int64_t)V < (int64_t)cs * PIECE) continue;
+        const int n = walk_clusters(cs);
+        if (n <= 0) continue;
+        if (n >= B) return cs;
+        if (fallback == 0) fallback = cs;
+    }
+    return fallback;
 }
 
 size_t stoch_ws_sums(int B, int V) { return align256((size_t)B * ((V + PIECE - 1) / PIECE) * 8); }
@@ -1013,25 +1070,21 @@ tv_status launch_accept(const AcceptArgs& a) {
         const int64_t R = (int64_t)a.B * a.N;
         static int64_t cap = -1;
         if (cap < 0) cap = resident_ctas(accept_rows_kernel<true>, ROWS_SMEM, sms);
-        const int ch = chunks_for(R, a.V, cap);
+        const int ch = std::min(32, chunks_for(R, a.V, cap));  // one chunk per lane when reduced
         if (R * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
         const RowsWs w = rows_ws(a.B, a.N);
         int2* part = reinterpret_cast<int2*>(ws + w.part);
-        int32_t* am = reinterpret_cast<int32_t*>(ws + w.am);
-        int32_t* rt = reinterpret_cast<int32_t*>(ws + w.row_tick);
         int32_t* st = reinterpret_cast<int32_t*>(ws + w.seq_tick);
         LaunchCfg lc(dim3((unsigned)(R * ch)), dim3(CH_THREADS), vec ? ROWS_SMEM : 0, a.stream);
-        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<true>, p, ch, part, am, rt, st)
-                : cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<false>, p, ch, part, am, rt, st);
+        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<true>, p, ch, part, st)
+                : cudaLaunchKernelEx(&lc.cfg, accept_rows_kernel<false>, p, ch, part, st);
     } else if (a.mode == TV_ACCEPT_GREEDY) {
-        const bool large = enable_large_clusters();
-        int C = ((int64_t)a.B * 16 <= 2LL * sms) ? 16 : 8;
-        if (!large && C > 8) C = 8;
-        while (C > 1 && C > a.V / 4) C >>= 1;  // keep every slice non-trivial on tiny vocabularies
+        const int C = walk_cluster_size(a.B, a.V);
+        if (C <= 0) return TV_ERR_CUDA;
         if ((int64_t)a.B * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
-        LaunchCfg lc(dim3((unsigned)(a.B * C)), dim3(ACC_THREADS), 0, a.stream, (unsigned)C);
-        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<true>, p)
-                : cudaLaunchKernelEx(&lc.cfg, accept_greedy_kernel<false>, p);
+        LaunchCfg lc(dim3((unsigned)(a.B * C)), dim3(CH_THREADS), 0, a.stream, (unsigned)C);
+        e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_walk_kernel<true>, p)
+                : cudaLaunchKernelEx(&lc.cfg, accept_walk_kernel<false>, p);
     } else {
         static int64_t cap = -1;
         if (!stoch_attr()) return TV_ERR_CUDA;
