@@ -353,8 +353,10 @@ def run_ours(args):
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else None
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     alg = {1: attn_bytes(w), 2: accept_bytes(w, acc_len)}.get(dom)
-    files = {0: "tree_mask.cu", 1: "attn_bf16.cu" if bf else "attn_f32.cu", 2: "accept.cu",
-             3: "kv_compact.cu"}
+    G = s.Hq // s.Hkv
+    tc = bf and s.d == 128 and G <= 128 and N * G > 64  # the tensor-memory attention kernel
+    files = {0: "tree_mask.cu", 1: ("attn_tc.cu" if tc else "attn_bf16.cu") if bf else "attn_f32.cu",
+             2: "accept.cu", 3: "kv_compact.cu"}
     if alg is None:
         # mask / compaction: bytes moved by the definition
         alg = (B * N * 4 + B * N * 12) if dom == 0 else \
