@@ -66,10 +66,18 @@ __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     const int lane = threadIdx.x & 31;
     bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
     if (ok) {
+        // four independent loads per lane in flight per round
         const int nb = (P + p.N + p.bs - 1) / p.bs;
-        for (int j = lane; j < nb; j += 32) {
-            const int blk = p.table[(int64_t)b * p.max_blocks + j];
-            ok = ok && blk >= 0 && blk < p.num_blocks;
+        const int32_t* row = p.table + (int64_t)b * p.max_blocks;
+        for (int j0 = 0; j0 < nb; j0 += 128) {
+            int blk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * 32 + lane;
+                blk[u] = (j < nb) ? row[j] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ok = ok && blk[u] >= 0 && blk[u] < p.num_blocks;
         }
     }
     return __all_sync(0xffffffffu, ok);
@@ -162,7 +170,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
     cluster_barrier_all();
     pdl_wait();  // everything above touched only shared memory
     const int* order = nullptr;
-    if (p.B <= LPT_MAX) {
+    if (p.B > 1 && p.B <= LPT_MAX) {
         lpt_order(p.prefix_lens, p.B, lpt, lpt + LPT_MAX);
         order = lpt + LPT_MAX;
     }
@@ -181,9 +189,12 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
             // rank 0 fetches the next group id and hands it to the whole cluster
             // (the producer warp also validates the group's sequence, once)
             if (rank == 0) {
+                // the first group of every cluster is its cluster index; later ones
+                // come from the counter, after the clusters' first groups
                 int gi = p.groups;
                 if (lane == 0 && mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u))
-                    gi = atomicAdd(&p.sched[0], 1);
+                    gi = (k == 0) ? (int)(blockIdx.x / cs)
+                                  : (int)(gridDim.x / cs) + atomicAdd(&p.sched[0], 1);
                 gi = __shfl_sync(0xffffffffu, gi, 0);
                 int word = gi;
                 if (gi < p.groups) {

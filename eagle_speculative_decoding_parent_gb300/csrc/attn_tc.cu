@@ -92,10 +92,18 @@ __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     const int lane = threadIdx.x & 31;
     bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
     if (ok) {
+        // four independent loads per lane in flight per round
         const int nb = (P + p.N + p.bs - 1) / p.bs;
-        for (int j = lane; j < nb; j += 32) {
-            const int blk = p.table[(int64_t)b * p.max_blocks + j];
-            ok = ok && blk >= 0 && blk < p.num_blocks;
+        const int32_t* row = p.table + (int64_t)b * p.max_blocks;
+        for (int j0 = 0; j0 < nb; j0 += 128) {
+            int blk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = j0 + u * 32 + lane;
+                blk[u] = (j < nb) ? row[j] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ok = ok && blk[u] >= 0 && blk[u] < p.num_blocks;
         }
     }
     return __all_sync(0xffffffffu, ok);
@@ -197,7 +205,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     pdl_wait();  // everything above touched only shared memory and TMEM
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_base_slot);
     const int* order = nullptr;
-    if (p.B <= LPT_MAX) {
+    if (p.B > 1 && p.B <= LPT_MAX) {
         int* lpt = reinterpret_cast<int*>(smem + OFF_LPT);
         lpt_order(p.prefix_lens, p.B, lpt, lpt + LPT_MAX);
         order = lpt + LPT_MAX;
@@ -208,9 +216,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     auto next_group = [&](uint32_t k, bool fetcher) -> int {
         const int slot = k % GQ;
         if (fetcher) {
+            // the first group of every cluster is its cluster index; later ones come
+            // from the counter, after the clusters' first groups
+            const int nclusters = (int)(gridDim.x / cs);
             int gi = p.groups;
             if (lane == 0 && mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u))
-                gi = atomicAdd(&p.sched[0], 1);
+                gi = (k == 0) ? (int)(blockIdx.x / cs) : nclusters + atomicAdd(&p.sched[0], 1);
             gi = __shfl_sync(0xffffffffu, gi, 0);
             int word = gi;
             if (gi < p.groups) {
@@ -669,29 +680,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int rows_per = 128 / (int)cs;
             const int rb = (int)rank * rows_per;
             if (row < rows_per) {
+                // every rank's (max, sum) of this row, all loads in flight at once
                 const int lr = rb + row;
+                float2 ml[MAX_CS];
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c)
+                    ml[c] = (c < (int)cs) ? remote_ld_f2(reinterpret_cast<const float*>(&xml[lr]), c)
+                                          : make_float2(-INFINITY, 0.f);
                 float mx = -INFINITY;
-                for (uint32_t c = 0; c < cs; ++c) mx = fmaxf(mx, remote_ld_f2(reinterpret_cast<const float*>(&xml[lr]), c).x);
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c) mx = fmaxf(mx, ml[c].x);
                 const float bz = (mx == -INFINITY) ? 0.f : mx;
+                float w[MAX_CS];
                 float den = 0.f;
-                for (uint32_t c = 0; c < cs; ++c) {
-                    const float2 ml = remote_ld_f2(reinterpret_cast<const float*>(&xml[lr]), c);
-                    const float w = exp2f(ml.x - bz) * ml.y;
-                    wts[lr * MAX_CS + c] = w;
-                    den += w;
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c) {
+                    w[c] = (c < (int)cs) ? exp2f(ml[c].x - bz) * ml[c].y : 0.f;
+                    den += w[c];
                 }
                 const float inv = (den > 0.f) ? 1.f / den : 0.f;
-                for (uint32_t c = 0; c < cs; ++c) wts[lr * MAX_CS + c] *= inv;
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c)
+                    if (c < (int)cs) wts[lr * MAX_CS + c] = w[c] * inv;
             }
             named_bar_sync(2, 128);
             for (int e = row; e < rows_per * (D / 8); e += 128) {
                 const int lr = rb + e / (D / 8);
                 const int c8 = (e % (D / 8)) * 8;
                 float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                for (uint32_t c = 0; c < cs; ++c) {
+                uint4 xv[MAX_CS];
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c)  // every rank's 16 bytes in flight at once
+                    xv[c] = (c < (int)cs) ? remote_ld_u4(xo + lr * (D * 2) + c8 * 2, c)
+                                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < MAX_CS; ++c) {
+                    if (c >= (int)cs) break;
                     const float w = wts[lr * MAX_CS + c];
-                    const uint4 v = remote_ld_u4(xo + lr * (D * 2) + c8 * 2, c);
-                    const __half2* h = reinterpret_cast<const __half2*>(&v);
+                    const __half2* h = reinterpret_cast<const __half2*>(&xv[c]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 f2 = __half22float2(h[q]);
