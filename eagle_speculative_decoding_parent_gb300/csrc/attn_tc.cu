@@ -67,7 +67,7 @@ constexpr int Q_BYTES = 128 * D * 2;                   // 32 KB
 constexpr int OFF_XML = OFF_Q + Q_BYTES;               // (max, sum) per row
 constexpr int OFF_WTS = OFF_XML + 128 * 8;             // merge weights [128][MAX_CS]
 constexpr int OFF_BARS = OFF_WTS + 128 * MAX_CS * 4;
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 2 + 2 * GQ + 2;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 2 * GQ + 2;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_LPT = OFF_MISC + 64;                 // sequence order: lens, order
 constexpr int SMEM_BYTES = OFF_LPT + 2 * LPT_MAX * 4 + 1024;  // + alignment slack
@@ -150,9 +150,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* sfull = qempty + 1;             // [2]
     uint64_t* sfree = sfull + 2;              // [2]
     uint64_t* pfull = sfree + 2;              // [2]
-    uint64_t* pfree = pfull + 2;              // [2]
-    uint64_t* pvdone = pfree + 2;             // [2] PV product of tile t done (by t & 1)
-    uint64_t* ofree = pvdone + 2;
+    uint64_t* pfree = pfull + 2;              // [2] PV product of tile t done (by t & 1)
+    uint64_t* ofree = pfree + 2;
     uint64_t* tailb = ofree + 1;
     uint64_t* gq_full = tailb + 1;            // [GQ]
     uint64_t* gq_empty = gq_full + GQ;        // [GQ]
@@ -182,8 +181,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&pfull[i], 4);
             mbar_init(&pfree[i], 1);
         }
-        mbar_init(&pvdone[0], 1);
-        mbar_init(&pvdone[1], 1);
         mbar_init(ofree, 4);
         mbar_init(tailb, 2);
         for (int s = 0; s < GQ; ++s) {
@@ -438,7 +435,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 tc_commit_elect(&kempty[s]);
                 tc_commit_elect(&pfree[pb]);
-                tc_commit_elect(&pvdone[gt & 1]);
                 __syncwarp();
             }
             if (!alive) break;
@@ -454,19 +450,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         float2* xml = reinterpret_cast<float2*>(smem + OFF_XML);
         float* wts = reinterpret_cast<float*>(smem + OFF_WTS);
         uint32_t gt = 0, merges = 0;
-        uint32_t pv_seen = 0;  // PV completions consumed, strictly in order (parity waits)
         bool alive = true;
-        // waits until the PV products of tiles < upto are complete, one phase at a time;
-        // tile t's completion is phase t / 2 of pvdone[t & 1], so a barrier is never
-        // more than one phase ahead as long as PV(t - 2) is consumed before P(t) is
-        // published
-        auto consume_pv = [&](uint32_t upto) -> bool {
-            bool ok = true;
-            while (ok && pv_seen < upto) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[pv_seen & 1u], (pv_seen >> 1) & 1u));
-                ++pv_seen;
-            }
-            return ok;
+        // waits until the PV product of tile t (and so every earlier one) is complete:
+        // that is phase t / 2 of pfree[t & 1].  Called only while P(t + 2) is not yet
+        // published, so the barrier cannot have moved a second phase past it.
+        auto wait_pv = [&](uint32_t t) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(&pfree[t & 1u], (t >> 1) & 1u));
         };
         for (uint32_t k = 0;; ++k) {
             const int gi = next_group(k, false);
@@ -514,78 +503,60 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 }
                 const float csc = p.scale_log2;
-                uint32_t pk[KT / 2];
-                float rs[4] = {0.f, 0.f, 0.f, 0.f};
-                // Common case: the running max m_used stays within 2^8 of every score
-                // of this tile, so the exponentials need no tile maximum first.  The
-                // largest exponent is checked on the way; a warp with a row past the
-                // bound (or still without a max) redoes the tile below.
-                bool redo = (m_used == -INFINITY);
-                if (!__any_sync(0xffffffffu, redo)) {
-                    const float nbase = -m_used;
-                    float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                // row maximum of the raw scores (four chains of three-input maxima); the
+                // scale is folded into the exponent, so the scaled maximum is tmax * csc
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int c = 0; c < KT; c += 2) {
-                        const float xa = fmaf(sv[c], csc, nbase);
-                        const float xb = fmaf(sv[c + 1], csc, nbase);
-                        xm[(c >> 1) & 3] = fmaxf(xm[(c >> 1) & 3], fmaxf(xa, xb));
-                        const float a = ex2_approx(xa);
-                        const float b2 = ex2_approx(xb);
-                        rs[(c >> 1) & 3] += a + b2;
-                        pk[c / 2] = pack_bf16x2(a, b2);
-                    }
-                    redo = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) > RESCALE_LOG2;
-                }
-                if (__any_sync(0xffffffffu, redo)) {
-                    // row maximum as a tree of eight independent chains
-                    float mx[8];
+                for (int c = 0; c < KT; c += 8)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[i + 8]);
-#pragma unroll
-                    for (int c = 16; c < KT; c += 8)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], sv[c + i]);
-                    float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    tmax *= csc;  // scores stay unscaled; the scale is folded into the exponent
-                    const float m_new = fmaxf(m_used, tmax);
-                    const bool need = (m_used == -INFINITY) ? (m_new > -INFINITY)
-                                                            : (m_new > m_used + RESCALE_LOG2);
-                    if (__any_sync(0xffffffffu, need)) {
-                        const float f = (need && m_used > -INFINITY) ? exp2f(m_used - m_new) : 1.f;
-                        if (j > 0) {
-                            // O holds the products of earlier tiles: rescale it once they are done
-                            if (!consume_pv(gt)) {
-                                alive = false;
-                                break;
-                            }
-                            tc_fence_after();
-#pragma unroll
-                            for (int c = 0; c < D; c += 32) {
-                                uint32_t r[32];
-                                tmem_ld32(tO + c, r);
-                                tmem_wait_ld();
-#pragma unroll
-                                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-                                tmem_st32(tO + c, r);
-                            }
-                            tmem_wait_st();
+                    for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], sv[c + i], sv[c + 4 + i]);
+                const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * csc;
+                // The running max m_used is raised only when a score passes it by more
+                // than 2^8 (or a row has none yet); a warp with such a row rescales O.
+                const bool need = (m_used == -INFINITY) ? (tmax > -INFINITY)
+                                                        : (tmax > m_used + RESCALE_LOG2);
+                if (__any_sync(0xffffffffu, need)) {
+                    const float f = (need && m_used > -INFINITY) ? exp2f(m_used - tmax) : 1.f;
+                    if (j > 0) {
+                        // O holds the products of earlier tiles: rescale it once they are done
+                        if (!wait_pv(gt - 1)) {
+                            alive = false;
+                            break;
                         }
-                        l *= f;
-                        if (need) m_used = m_new;
-                    }
-                    const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
+                        tc_fence_after();
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) rs[i] = 0.f;
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t r[32];
+                            tmem_ld32(tO + c, r);
+                            tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < KT; c += 2) {
-                        const float a = ex2_approx(fmaf(sv[c], csc, nbase));
-                        const float b2 = ex2_approx(fmaf(sv[c + 1], csc, nbase));
-                        rs[(c >> 1) & 3] += a + b2;
-                        pk[c / 2] = pack_bf16x2(a, b2);
+                            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+                            tmem_st32(tO + c, r);
+                        }
+                        tmem_wait_st();
                     }
+                    l *= f;
+                    if (need) m_used = tmax;
                 }
-                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                // P = 2^(s * csc - m_used), two keys per packed fp32 pair instruction
+                const float nbase = (m_used == -INFINITY) ? 0.f : -m_used;
+                const uint64_t sc2 = f2_pack(csc, csc), nb2 = f2_pack(nbase, nbase);
+                uint32_t pk[KT / 2];
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed (0.f, 0.f)
+#pragma unroll
+                for (int c = 0; c < KT; c += 2) {
+                    float xa, xb;
+                    f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), sc2, nb2), xa, xb);
+                    const float a = ex2_approx(xa);
+                    const float b2 = ex2_approx(xb);
+                    acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(a, b2));
+                    pk[c / 2] = pack_bf16x2(a, b2);
+                }
+                {
+                    float lo, hi;
+                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), lo, hi);
+                    l += lo + hi;
+                }
                 // P row -> tensor memory (this thread's lane) once its buffer is free
                 const int pb = gt & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(&pfree[pb], ((gt >> 1) & 1u) ^ 1u))) {
@@ -594,11 +565,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 tmem_st32(tmem + lane_off + TMEM_P + pb * (KT / 2), pk);
                 tmem_wait_st();
-                // PV(gt - 2) shares a completion barrier with PV(gt): consume it first
-                if (gt >= 2 && !consume_pv(gt - 1)) {
-                    alive = false;
-                    break;
-                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&pfull[pb]);
@@ -615,7 +581,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 break;
             }
             if (n > 0) {
-                if (!consume_pv(gt)) {
+                if (!wait_pv(gt - 1)) {
                     alive = false;
                     break;
                 }
