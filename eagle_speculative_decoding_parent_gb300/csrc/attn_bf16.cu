@@ -714,13 +714,15 @@ tv_status launch_typed(const AttnArgs& a, const CUtensorMap& km, const CUtensorM
 }  // namespace
 
 size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs) {
-    (void)B; (void)N; (void)Hq; (void)Hkv; (void)d; (void)max_blocks; (void)bs;
+    (void)max_blocks; (void)bs;
+    if (attn_tc_applicable(N, Hq, Hkv, d)) return attn_tc_workspace(B, N, Hq, Hkv);
     return kSchedBytes;
 }
 
 size_t attn_bf16_workspace_zeroed_prefix(int B, int N, int Hq, int Hkv, int d, int max_blocks,
                                          int bs) {
-    (void)B; (void)N; (void)Hq; (void)Hkv; (void)d; (void)max_blocks; (void)bs;
+    (void)max_blocks; (void)bs;
+    if (attn_tc_applicable(N, Hq, Hkv, d)) return attn_tc_zeroed_prefix(B, N, Hq, Hkv);
     return kSchedBytes;
 }
 

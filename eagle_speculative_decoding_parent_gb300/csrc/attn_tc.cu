@@ -1,23 +1,32 @@
 // tree_verify_attention, bfloat16 path on the 5th-generation tensor cores.
 //
 // Used when the packed row tile is a real dense contraction (more than 64
-// rows).  Same work decomposition as the warp-MMA kernel: a group is
-// (sequence, kv head, row tile); groups go dynamically to clusters of CS CTAs
-// that split the group's keys and merge through distributed shared memory.
+// rows).  A group is (sequence, kv head, row tile).  Two schedules:
+//   balanced split (when the caller's workspace holds the partial results):
+//            the grid is QT CTAs (one per row tile) times `lanes`; the key
+//            tiles of all (sequence, kv head) pairs, laid end to end, are cut
+//            into `lanes` runs of equal length, so every CTA streams the same
+//            number of tiles.  A group cut by a run boundary leaves one partial
+//            result (running max, sum, normalised O) per run in global memory,
+//            and the last run to finish, seen from an arrival counter, merges
+//            them.
+//   clusters (otherwise): groups go dynamically to clusters of CS CTAs that
+//            split the group's keys and merge through distributed shared memory.
 // A row tile holds npt = floor(128 / G) whole nodes (all G query heads of the
 // kv head for each), rows r = node * G + head, so one TMA box loads it.
 //
 // CTA roles (256 threads, one CTA per SM)
-//   warp 0   producer of Q (3-D TMA box per row tile) and of pages 0-1 of
-//            each 64-key K/V tile; warp 2 loads pages 2-3.  A 16-key page is
+//   warp 0   producer of pages 0-1 of each 64-key K/V tile; warp 2 loads
+//            pages 2-3.  A 16-key page is
 //            two K boxes (one per 64-column half) and one V box holding both
 //            halves; the ring has 5 stages (4 when a cluster splits the group).
-//            Warp 0 of rank 0 also fetches group ids for the cluster and
-//            validates each group's block table; warp 2 also allocates / frees
-//            512 tensor-memory columns: S double buffer (2 x 64), O (128), P
-//            (2 x 32).
-//   warp 1   S issuer: S = Q K^T into tensor memory (M=128, N=64, K=16 steps,
-//            both operands in shared memory), double-buffered S.
+//            Warp 0 of rank 0 also hands out the work items; warp 2 allocates /
+//            frees 512 tensor-memory columns: S double buffer (2 x 64), O (128),
+//            P (2 x 32).
+//   warp 1   S issuer: loads each group's Q tile (3-D TMA box) once the
+//            previous group's S products are done with it, so the K/V stream
+//            runs on across groups; S = Q K^T into tensor memory (M=128, N=64,
+//            K=16 steps, both operands in shared memory), double-buffered S.
 //   warp 3   PV issuer: O += P V (M=128, N=128, P read from tensor memory, V
 //            N-major in shared memory), in tile order; releases the K/V stage.
 //            Completion is signalled with tcgen05.commit (it covers only the
@@ -29,6 +38,11 @@
 //            raised (and O rescaled in tensor memory) when it grows by more
 //            than 2^8, writes P (bf16 pairs) to tensor memory for the PV
 //            product, and finally normalises O.
+// Balanced split: before the roles start, the CTA lists its run's pieces (up
+// to MAXI) and checks the block tables of their sequences with every warp at
+// once; the producers load each next piece's first block ids while the
+// current one streams.  So no global-memory round trip sits between pieces
+// but the K/V data itself.
 #include <algorithm>
 
 #include "tv_device.cuh"
@@ -70,7 +84,20 @@ constexpr int OFF_BARS = OFF_WTS + 128 * MAX_CS * 4;
 constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 2 * GQ + 2;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_LPT = OFF_MISC + 64;                 // sequence order: lens, order
-constexpr int SMEM_BYTES = OFF_LPT + 2 * LPT_MAX * 4 + 1024;  // + alignment slack
+constexpr int OFF_CUM = OFF_LPT + 2 * LPT_MAX * 4;     // balanced split: int64 [LPT_MAX + 1]
+constexpr int OFF_GQT = OFF_CUM + (LPT_MAX + 1) * 8 + 8;  // key-tile range per queue slot [GQ][2]
+constexpr int MAXI = 64;                               // balanced split: pieces listed up front
+constexpr int OFF_ITEMS = OFF_GQT + GQ * 8;            // [MAXI] x (word, first tile, end tile, bad)
+constexpr int OFF_NITEMS = OFF_ITEMS + MAXI * 16;
+constexpr int SMEM_BYTES = OFF_NITEMS + 16 + 1024;     // + alignment slack
+static_assert(OFF_CUM % 8 == 0, "int64 prefix sums");
+static_assert(OFF_ITEMS % 16 == 0, "int4 items");
+// Balanced split: cost of starting a piece (Q tile, pipeline fill and drain,
+// epilogue), in key-tile times.
+constexpr int SPLIT_C0 = 4;
+// one partial result in the workspace: fp16 normalised O rows, then (max, sum) per row
+constexpr int SLOT_O_BYTES = 128 * D * 2;
+constexpr int SLOT_BYTES = SLOT_O_BYTES + 128 * 8;
 
 struct Params {
     const int32_t* table;
@@ -79,14 +106,69 @@ struct Params {
     __nv_bfloat16* out;
     int32_t* status;
     int32_t* sched;
+    uint8_t* part;         // balanced split: 2 partial-result slots per CTA
     int max_blocks, B, N, Hq, Hkv, G, npt, bs, num_blocks, QT, groups;
+    int lanes;             // balanced split: grid = lanes * QT, no clusters
+    int c0;                // balanced split: fixed cost of a piece, in key tiles
     float scale_log2;
 };
 
 struct Group {
     int b, g, qt, P, L, t_lo, t_hi;
     bool ok;
+    bool whole;            // the piece covers all of the group's key tiles
 };
+
+// A fetched work item: group word and, for the balanced split, its key tiles.
+struct Item {
+    int word, t_lo, t_hi;
+};
+
+// Balanced split: the run space.  Group (b, g) takes c0 + T_b units, c0 for
+// the fixed cost of starting a piece and then one per key tile; cum[0..B] is
+// the exclusive prefix sum over sequences (Hkv groups each), and lens[b] the
+// prefix length.  A sequence whose prefix length is out of range counts one
+// tile, so that one CTA owns it and reports it.  Called by every thread of the
+// CTA; B <= LPT_MAX.
+__device__ __forceinline__ void split_prefix(const Params& p, int64_t* cum, int* lens) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int64_t v[LPT_MAX / 32];
+#pragma unroll
+        for (int u = 0; u < LPT_MAX / 32; ++u) {
+            const int b = u * 32 + lane;
+            v[u] = 0;
+            if (b < p.B) {
+                const int P = p.prefix_lens[b];
+                lens[b] = P;
+                const bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
+                v[u] = (int64_t)((ok ? (P + p.N + KT - 1) / KT : 1) + p.c0) * p.Hkv;
+            }
+        }
+        int64_t run = 0;
+#pragma unroll
+        for (int u = 0; u < LPT_MAX / 32; ++u) {
+            int64_t x = v[u];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int b = u * 32 + lane;
+            if (b < p.B) cum[b + 1] = run + x;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) cum[0] = 0;
+    }
+    __syncthreads();
+}
+
+// Balanced split: first tile of lane l's run among U tiles cut into L runs, and
+// the lane whose run holds tile x.
+__device__ __forceinline__ int64_t run_start(int64_t l, int64_t U, int64_t L) { return l * U / L; }
+__device__ __forceinline__ int64_t run_owner(int64_t x, int64_t U, int64_t L) {
+    return ((x + 1) * L - 1) / U;
+}
 
 __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     const int lane = threadIdx.x & 31;
@@ -120,22 +202,37 @@ __device__ __forceinline__ int group_seq(const Params& p, const int* order, int 
 
 // Fetched word -> group: sequence (in longest-first order when `order` is
 // given), kv head, row tile; this CTA's share of its key tiles.
-__device__ __forceinline__ Group decode_group(const Params& p, const int* order, int word, int rank,
-                                             int cs) {
+template <bool SPLIT>
+__device__ __forceinline__ Group decode_group(const Params& p, const int* order, const int* lens,
+                                             const int64_t* cum, const Item& it, int rank, int cs) {
     Group gr;
+    const int word = it.word;
     const int gi = word & (GROUP_BAD - 1);
     gr.qt = gi % p.QT;
     gr.g = (gi / p.QT) % p.Hkv;
     gr.b = group_seq(p, order, gi);
-    gr.P = p.prefix_lens[gr.b];
+    gr.P = lens ? lens[gr.b] : p.prefix_lens[gr.b];
     gr.L = gr.P + p.N;
     gr.ok = (word & GROUP_BAD) == 0;
     const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
-    gr.t_lo = (int)((int64_t)T * rank / cs);
-    gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
+    if constexpr (SPLIT) {
+        // a piece of a bad sequence reads nothing: a whole one writes zeros, a
+        // partial one an empty partial result (zero weight in the merge)
+        const int T_run = (int)((cum[gr.b + 1] - cum[gr.b]) / p.Hkv) - p.c0;
+        gr.t_lo = gr.ok ? it.t_lo : 0;
+        gr.t_hi = gr.ok ? it.t_hi : 0;
+        gr.whole = (it.t_lo == 0 && it.t_hi == T_run);
+    } else {
+        gr.t_lo = (int)((int64_t)T * rank / cs);
+        gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
+        gr.whole = (cs == 1);
+    }
     return gr;
 }
 
+// SPLIT: the balanced split (else the cluster schedule); one instantiation
+// each, so that neither carries the other's code.
+template <bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, Params p) {
@@ -161,6 +258,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int* gq = misc;                           // [GQ]
     uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(misc + GQ);
     int* flags = misc + GQ + 1;               // [0] abort
+    int* gqt = reinterpret_cast<int*>(smem + OFF_GQT);  // [GQ][2] key tiles of the item
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), cs = cluster_size();
@@ -202,30 +300,181 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     pdl_wait();  // everything above touched only shared memory and TMEM
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_base_slot);
     const int* order = nullptr;
-    if (p.B > 1 && p.B <= LPT_MAX) {
-        int* lpt = reinterpret_cast<int*>(smem + OFF_LPT);
-        lpt_order(p.prefix_lens, p.B, lpt, lpt + LPT_MAX);
-        order = lpt + LPT_MAX;
+    const int64_t* cum = reinterpret_cast<const int64_t*>(smem + OFF_CUM);
+    // prefix lengths in shared memory (every sequence fits the table)
+    int* lens_w = reinterpret_cast<int*>(smem + OFF_LPT);
+    const int* lens = (SPLIT || (p.B > 1 && p.B <= LPT_MAX)) ? lens_w : nullptr;
+    // balanced split: the run's pieces listed up front
+    int4* items = reinterpret_cast<int4*>(smem + OFF_ITEMS);  // word, first tile, end tile, bad
+    int* n_items = reinterpret_cast<int*>(smem + OFF_NITEMS);
+    int* items_more = n_items + 1;
+    // balanced split: this CTA's run [x_lo, x_hi) of the run space and its row tile
+    int64_t U = 0, L = 0, x_lo = 0, x_hi = 0;
+    int qt_me = 0;
+    if constexpr (SPLIT) {
+        split_prefix(p, reinterpret_cast<int64_t*>(smem + OFF_CUM), lens_w);
+        U = cum[p.B];
+        L = min((int64_t)p.lanes, U);  // every run holds at least one tile
+        const int64_t lane_me = blockIdx.x / p.QT;
+        qt_me = (int)(blockIdx.x % p.QT);
+        if (lane_me < L) {
+            x_lo = run_start(lane_me, U, L);
+            x_hi = run_start(lane_me + 1, U, L);
+        }
+    } else if (p.B > 1 && p.B <= LPT_MAX) {
+        lpt_order(p.prefix_lens, p.B, lens_w, lens_w + LPT_MAX);
+        order = lens_w + LPT_MAX;
     }
+    // balanced split: the run's pieces as (group, first tile, end tile).  A piece
+    // that starts in the run and continues into the next one goes first, so
+    // that the groups cut at both ends of the run are finished (and merged)
+    // early; then the rest of the run in order.  Group p.groups once done.
+    // (the fetching warp only)
+    int64_t x_next = x_lo, x_stop = x_hi;
+    bool z_first = false;
+    int z_word = 0, z_thi = 0;
+    auto split_locate = [&](int64_t x, int& b, int64_t& w, int64_t& g0) {
+        int lo = 0, hi = p.B;  // cum[lo] <= x < cum[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cum[mid] <= x) lo = mid;
+            else hi = mid;
+        }
+        b = lo;
+        w = (cum[lo + 1] - cum[lo]) / p.Hkv;   // c0 + tiles
+        g0 = x - (x - cum[lo]) % w;            // the group's first unit
+    };
+    if (SPLIT && x_hi > x_lo) {
+        int b;
+        int64_t w, g0;
+        split_locate(x_hi - 1, b, w, g0);
+        const int64_t f = g0 + p.c0, tb = w - p.c0;  // first tile unit, tiles
+        if (f >= x_lo && f < x_hi && f + tb > x_hi) {
+            z_first = true;
+            z_word = (b * p.Hkv + (int)((g0 - cum[b]) / w)) * p.QT + qt_me;
+            z_thi = (int)(x_hi - f);
+            x_stop = g0;
+        }
+    }
+    auto split_next = [&](int& word, int& tlo, int& thi) {
+        word = p.groups;
+        tlo = thi = 0;
+        if (z_first) {
+            z_first = false;
+            word = z_word;
+            thi = z_thi;
+            return;
+        }
+        while (x_next < x_stop) {
+            int b;
+            int64_t w, g0;
+            split_locate(x_next, b, w, g0);
+            const int64_t f = g0 + p.c0, tb = w - p.c0;
+            if (x_next < f) {
+                if (f >= x_stop) {  // the group's tiles all lie past this run
+                    x_next = x_stop;
+                    break;
+                }
+                x_next = f;
+            }
+            const int64_t t = x_next - f;
+            const int64_t take = min(tb - t, x_stop - x_next);
+            word = (b * p.Hkv + (int)((g0 - cum[b]) / w)) * p.QT + qt_me;
+            tlo = (int)t;
+            thi = (int)(t + take);
+            x_next += take;
+            return;
+        }
+    };
 
-    // group id k of this CTA (all roles walk the same sequence)
-    // (the fetcher is a whole warp: it also validates the group's sequence)
-    auto next_group = [&](uint32_t k, bool fetcher) -> int {
-        const int slot = k % GQ;
-        if (fetcher) {
-            // the first group of every cluster is its cluster index; later ones come
-            // from the counter, after the clusters' first groups
-            const int nclusters = (int)(gridDim.x / cs);
-            int gi = p.groups;
-            if (lane == 0 && mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u))
-                gi = (k == 0) ? (int)(blockIdx.x / cs) : nclusters + atomicAdd(&p.sched[0], 1);
-            gi = __shfl_sync(0xffffffffu, gi, 0);
-            int word = gi;
-            if (gi < p.groups) {
-                const int b = group_seq(p, order, gi);
-                if (!seq_ok_warp(p, b, p.prefix_lens[b])) word |= GROUP_BAD;
+    if constexpr (SPLIT) {
+        // the run's pieces, in the order they will be handed out (warp 0 keeps the
+        // state for any pieces past the list)
+        if (warp == 0) {
+            int n = 0;
+            while (n < MAXI) {
+                int gi, tlo, thi;
+                split_next(gi, tlo, thi);
+                if (gi >= p.groups) break;
+                if (lane == 0) items[n] = make_int4(gi, tlo, thi, 0);
+                ++n;
             }
             if (lane == 0) {
+                *n_items = n;
+                *items_more = (n == MAXI) ? 1 : 0;
+            }
+        }
+        __syncthreads();
+        // block tables of the listed pieces' sequences, in units of 512 block ids
+        // spread over all warps (16 loads per lane in flight)
+        {
+            const int n = *n_items;
+            int u = 0;
+            for (int i = 0; i < n; ++i) {
+                const int b = group_seq(p, nullptr, items[i].x);
+                const int P = lens[b];
+                const bool pok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
+                const int nb = pok ? (P + p.N + p.bs - 1) / p.bs : 0;
+                const int chunks = max(1, (nb + 511) / 512);
+                for (int c = 0; c < chunks; ++c, ++u) {
+                    if (u % (THREADS / 32) != warp) continue;
+                    bool ok = pok;
+                    if (ok) {
+                        const int32_t* row = p.table + (int64_t)b * p.max_blocks;
+                        int blk[16];
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) {
+                            const int j = c * 512 + v * 32 + lane;
+                            blk[v] = (j < nb) ? row[j] : 0;
+                        }
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) ok = ok && blk[v] >= 0 && blk[v] < p.num_blocks;
+                    }
+                    if (!__all_sync(0xffffffffu, ok) && lane == 0) atomicOr(&items[i].w, 1);
+                }
+            }
+        }
+        __syncthreads();
+        if (tid < *n_items && items[tid].w) items[tid].x |= GROUP_BAD;
+        __syncthreads();
+    }
+
+    // work item k of this CTA (all roles walk the same sequence)
+    // (the fetcher is a whole warp: it also validates the group's sequence)
+    auto next_group = [&](uint32_t k, bool fetcher) -> Item {
+        const int slot = k % GQ;
+        if (fetcher) {
+            int gi = p.groups, tlo = 0, thi = 0, word = p.groups;
+            const bool free_slot = __all_sync(
+                0xffffffffu, lane != 0 || mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u));
+            if (!free_slot) {
+                // timed out: hand out the end marker
+            } else if (SPLIT && (int)k < *n_items) {
+                word = items[k].x;  // listed and checked in the prologue
+                tlo = items[k].y;
+                thi = items[k].z;
+            } else {
+                if constexpr (SPLIT) {
+                    if (!*items_more) gi = p.groups;
+                    else split_next(gi, tlo, thi);
+                } else {
+                    // the first group of every cluster is its cluster index; later ones
+                    // come from the counter, after the clusters' first groups
+                    const int nclusters = (int)(gridDim.x / cs);
+                    if (lane == 0)
+                        gi = (k == 0) ? (int)(blockIdx.x / cs)
+                                      : nclusters + atomicAdd(&p.sched[0], 1);
+                    gi = __shfl_sync(0xffffffffu, gi, 0);
+                }
+                word = gi;
+                if (gi < p.groups) {
+                    const int b = group_seq(p, order, gi);
+                    if (!seq_ok_warp(p, b, lens ? lens[b] : p.prefix_lens[b])) word |= GROUP_BAD;
+                }
+            }
+            if (lane == 0) {
+                gqt[2 * slot] = tlo;  // balanced split only: no cluster peers
+                gqt[2 * slot + 1] = thi;
                 for (uint32_t r = 0; r < cs; ++r) {
                     remote_st_u32(&gq[slot], r, word);
                     remote_arrive(&gq_full[slot], r);
@@ -233,10 +482,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             }
         }
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&gq_full[slot], (k / GQ) & 1u));
-        const int gi = got ? *(volatile int*)&gq[slot] : p.groups;
+        Item it;
+        it.word = got ? *(volatile int*)&gq[slot] : p.groups;
+        it.t_lo = *(volatile int*)&gqt[2 * slot];
+        it.t_hi = *(volatile int*)&gqt[2 * slot + 1];
         __syncwarp();
         if (lane == 0) remote_arrive(&gq_empty[slot], 0);
-        return gi;
+        return it;
     };
 
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -250,36 +502,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const bool kprod = (warp == 0);
         const int pg0 = kprod ? 0 : KT / 32;
         if (lane == 0) {
-            if (kprod) tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
         }
         const uint64_t policy = (p.QT == 1) ? l2_policy_evict_first() : l2_policy_evict_normal();
-        uint32_t gt = 0, qi = 0, tail_phase = 0;
+        uint32_t gt = 0, tail_phase = 0;
         bool alive = true;
+        // balanced split: block id of page `lane` of listed piece pf_k, loaded one
+        // piece ahead
+        int pf_blk = 0, pf_k = -1;
         for (uint32_t k = 0; alive; ++k) {
-            const int gi = next_group(k, kprod && rank == 0);
-            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group(p, order, gi, rank, cs);
+            const Item it = next_group(k, kprod && rank == 0);
+            if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
+            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
-            if (kprod) {
-                // Q tile: npt nodes x G heads x 128 columns
-                if (lane == 0) {
-                    bool ok = mbar_wait(qempty, (qi & 1u) ^ 1u);
-                    if (!ok) {
-                        flags[0] = 1;
-                        p.status[gr.b] = TV_ERR_TIMEOUT;
-                    }
-                    const uint32_t qbytes = 2u * 64u * (uint32_t)(p.G * p.npt) * 2u;
-                    mbar_arrive_expect_tx(qfull, qbytes);
-                    const int node0 = gr.b * p.N + gr.qt * p.npt;
-                    for (int hf = 0; hf < 2; ++hf)
-                        tma_load_3d(smem + OFF_Q + hf * (128 * 128), &qmap, qfull, hf * 64,
-                                    gr.g * p.G, node0);
-                }
-                ++qi;
-            }
             // cache rows of the group's 16-key pages, 32 pages (8 tiles) per window:
             // lane l holds page l of the current window as a row index, and the
             // block id (loaded 8 tiles ahead) and row-in-block of the next window
@@ -293,8 +530,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             auto row_of = [&]() -> int { return (nxt_blk * p.Hkv + gr.g) * p.bs + nxt_off; };
             int win_y = 0;
             if (gr.t_lo < gr.t_hi) {
-                load_window(0);
+                if (pf_k == (int)k) {  // loaded while the previous piece streamed
+                    nxt_blk = pf_blk;
+                    nxt_off = ((gr.t_lo * (KT / 16) + lane) * 16) % p.bs;
+                } else {
+                    load_window(0);
+                }
                 win_y = row_of();
+            }
+            if (SPLIT && (int)k + 1 < *n_items) {
+                const int4 nx = items[k + 1];
+                if (!(nx.x & GROUP_BAD)) {
+                    const int gi = nx.x;
+                    const int nb_ = group_seq(p, nullptr, gi);
+                    const int tk = (nx.y * (KT / 16) + lane) * 16;
+                    pf_blk = (tk < lens[nb_] + p.N)
+                                 ? __ldg(p.table + (int64_t)nb_ * p.max_blocks + tk / p.bs)
+                                 : 0;
+                    pf_k = (int)k + 1;
+                }
             }
             if (gr.t_lo + WIN_TILES < gr.t_hi) load_window(1);
             for (int t = gr.t_lo; t < gr.t_hi; ++t, ++gt) {
@@ -375,13 +629,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ===================== S issuer: S = Q K^T per tile =====================
         uint32_t gt = 0, qi = 0;
         const uint32_t tS = tmem;
+        const uint64_t qpol = l2_policy_evict_normal();
+        if (lane == 0) tma_prefetch_desc(&qmap);
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
-            const int gi = next_group(k, false);
-            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group(p, order, gi, rank, cs);
+            const Item it = next_group(k, false);
+            if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
+            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
+            // Q tile (npt nodes x G heads x 128 columns) of this group, loaded here
+            // once the previous group's S products are done with the buffer, so
+            // the K/V producers never wait for it
+            if (!wait_all(qempty, (qi & 1u) ^ 1u)) { alive = false; break; }
+            {
+                const uint32_t qbytes = 2u * 64u * (uint32_t)(p.G * p.npt) * 2u;
+                const int node0 = gr.b * p.N + gr.qt * p.npt;
+                mbar_arrive_expect_tx_elect(qfull, qbytes);
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_load_3d_elect(smem + OFF_Q + hf * (128 * 128), &qmap, qfull, hf * 64,
+                                      gr.g * p.G, node0, qpol);
+            }
             if (!wait_all(qfull, qi & 1u)) { alive = false; break; }
             ++qi;
             for (int j = 0; j < n; ++j, ++gt) {
@@ -413,9 +681,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const uint32_t tO = tmem + TMEM_O;
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
-            const int gi = next_group(k, false);
-            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group(p, order, gi, rank, cs);
+            const Item it = next_group(k, false);
+            if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
+            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
             for (int j = 0; j < n; ++j, ++gt) {
@@ -458,9 +726,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             return __all_sync(0xffffffffu, mbar_wait(&pfree[t & 1u], (t >> 1) & 1u));
         };
         for (uint32_t k = 0;; ++k) {
-            const int gi = next_group(k, false);
-            if ((gi & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group(p, order, gi, rank, cs);
+            const Item it = next_group(k, false);
+            if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
+            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
             const int n = gr.t_hi - gr.t_lo;
@@ -575,6 +843,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             __nv_bfloat16* orow = nullptr;
             if (valid)
                 orow = p.out + (((int64_t)gr.b * p.N + node) * p.Hq + gr.g * p.G + head) * D;
+            // balanced split, a piece of a group: its slot (the first piece of this
+            // run if the group began in an earlier run, else the last)
+            const bool spiece = SPLIT && !gr.whole;
+            uint8_t* pbase = nullptr;
+            if (spiece) {
+                const int64_t w = (cum[gr.b + 1] - cum[gr.b]) / p.Hkv;
+                const int64_t F = cum[gr.b] + (int64_t)gr.g * w + p.c0;  // first tile unit
+                const int64_t lane_me = blockIdx.x / p.QT;
+                const int64_t slot = 2 * (int64_t)blockIdx.x + (F < run_start(lane_me, U, L) ? 0 : 1);
+                pbase = p.part + slot * SLOT_BYTES;
+            }
             if (cs > 1 && merges > 0 &&
                 !__all_sync(0xffffffffu, mbar_wait_cluster(xfree, (merges - 1) & 1u))) {
                 alive = false;
@@ -597,7 +876,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = 0u;
                 }
-                if (cs == 1) {
+                if (gr.whole) {
                     if (valid) {
 #pragma unroll
                         for (int e = 0; e < 32; e += 8) {
@@ -611,7 +890,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     }
                 } else {
                     // normalised row, fp16, into this CTA's exchange buffer (16-byte chunks)
-                    uint8_t* xr = xo + row * (D * 2);
+                    // or, for a balanced-split piece, into its workspace slot
+                    uint8_t* xr = spiece ? pbase + row * (D * 2) : xo + row * (D * 2);
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         __half2 h0 = __floats2half2_rn(__uint_as_float(r[e]) * o_inv, __uint_as_float(r[e + 1]) * o_inv);
@@ -632,7 +912,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ofree);  // O may be overwritten by the next group
             }
-            if (cs == 1) continue;
+            if (gr.whole) continue;
+            if (spiece) {
+                // balanced split: the piece is complete; the merge kernel that follows
+                // combines the group's pieces
+                reinterpret_cast<float2*>(pbase + SLOT_O_BYTES)[row] = make_float2(m_used, l);
+                continue;
+            }
             // ---- cluster merge: this CTA finishes rows [rank*128/cs, (rank+1)*128/cs)
             xml[row] = make_float2(m_used, l);
             asm volatile("fence.acq_rel.cluster;" ::: "memory");
@@ -730,6 +1016,155 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 }
 
 
+// Balanced split, second kernel: one CTA per (run boundary l = 1 .. L-1, row
+// tile).  The boundary at run_start(l) cuts at most one group's key tiles; the
+// CTA of the first boundary inside a group merges all of the group's pieces,
+// row by row: weights 2^(m_k - max) l_k / (sum over the pieces) on their
+// normalised partial outputs.
+constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_MW = 16;  // pieces whose weights sit in shared memory
+
+__global__ void __launch_bounds__(MERGE_THREADS)
+attn_split_merge_kernel(Params p) {
+    __shared__ int64_t cum[LPT_MAX + 1];
+    __shared__ int lens[LPT_MAX];
+    __shared__ float2 nz[128];                // per row: max, 1 / weighted sum
+    __shared__ float pw[MERGE_MW][128];       // weights of the first MERGE_MW pieces
+    __shared__ int pslot[MERGE_MW];
+    pdl_launch_dependents();
+    split_prefix(p, cum, lens);  // from the call's inputs: overlaps the attention kernel
+    const int tid = threadIdx.x;
+    const int64_t U = cum[p.B];
+    const int64_t L = min((int64_t)p.lanes, U);
+    const int64_t l = blockIdx.x / p.QT + 1;
+    const int qt = (int)(blockIdx.x % p.QT);
+    if (l >= L) return;
+    const int64_t x = run_start(l, U, L);
+    int b = 0, hi = p.B;  // cum[b] <= x < cum[hi]
+    while (hi - b > 1) {
+        const int mid = (b + hi) >> 1;
+        if (cum[mid] <= x) b = mid;
+        else hi = mid;
+    }
+    const int64_t w = (cum[b + 1] - cum[b]) / p.Hkv;
+    const int64_t g0 = x - (x - cum[b]) % w;
+    const int64_t F = g0 + p.c0, tb = w - p.c0;  // the group's first tile unit, tiles
+    if (x <= F || run_start(l - 1, U, L) > F) return;  // not cut here first
+    const int g = (int)((g0 - cum[b]) / w);
+    const int64_t l1 = run_owner(F + tb - 1, U, L);
+    const int pieces = (int)(l1 - (l - 1) + 1);
+    auto slot_of = [&](int k) -> int64_t {
+        const int64_t ln = l - 1 + k;
+        return 2 * (ln * p.QT + qt) + (F < run_start(ln, U, L) ? 0 : 1);
+    };
+    for (int k = tid; k < pieces && k < MERGE_MW; k += MERGE_THREADS) pslot[k] = (int)slot_of(k);
+    pdl_wait();  // the attention kernel's partial results are complete
+    __syncthreads();
+    const uint8_t* part = p.part;
+    auto slot_k = [&](int k) -> int64_t { return (k < MERGE_MW) ? pslot[k] : slot_of(k); };
+    auto ml_of = [&](int k, int r) -> float2 {
+        return __ldcg(reinterpret_cast<const float2*>(part + slot_k(k) * SLOT_BYTES + SLOT_O_BYTES) + r);
+    };
+    if (tid < 128) {
+        // row tid: max over the pieces, then the pieces' weights
+        const int r = tid;
+        float2 m8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m8[u] = (u < pieces) ? ml_of(u, r) : make_float2(-INFINITY, 0.f);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx = fmaxf(mx, m8[u].x);
+        for (int k = 8; k < pieces; ++k) mx = fmaxf(mx, ml_of(k, r).x);
+        const float bz = (mx == -INFINITY) ? 0.f : mx;
+        float e8[8], den = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            e8[u] = exp2f(m8[u].x - bz) * m8[u].y;
+            den += e8[u];
+        }
+        for (int k = 8; k < pieces; ++k) {
+            const float2 ml = ml_of(k, r);
+            den += exp2f(ml.x - bz) * ml.y;
+        }
+        const float inv = (den > 0.f) ? 1.f / den : 0.f;
+        nz[r] = make_float2(bz, inv);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (u < pieces) pw[u][r] = e8[u] * inv;
+        for (int k = 8; k < pieces && k < MERGE_MW; ++k) {
+            const float2 ml = ml_of(k, r);
+            pw[k][r] = exp2f(ml.x - bz) * ml.y * inv;
+        }
+    }
+    __syncthreads();
+    // 16-byte chunks of the 128 x D output tile: thread t takes t + 256 i (i < 8),
+    // with two pieces' loads of all eight chunks in flight together
+    constexpr int CH = 128 * (D / 8) / MERGE_THREADS;
+    constexpr int KB = 2;
+    int lr[CH], c8[CH];
+    bool ok[CH];
+#pragma unroll
+    for (int v = 0; v < CH; ++v) {
+        const int e = tid + MERGE_THREADS * v;
+        lr[v] = e / (D / 8);
+        c8[v] = (e % (D / 8)) * 8;
+        const int nl = lr[v] / p.G;
+        ok[v] = nl < p.npt && qt * p.npt + nl < p.N;
+    }
+    float acc[CH][8];
+#pragma unroll
+    for (int v = 0; v < CH; ++v)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[v][q] = 0.f;
+    for (int k0 = 0; k0 < pieces; k0 += KB) {
+        uint4 xv[KB][CH];
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            const int k = k0 + u;
+            const uint8_t* sb = (k < pieces) ? part + slot_k(k) * SLOT_BYTES : nullptr;
+#pragma unroll
+            for (int v = 0; v < CH; ++v)
+                xv[u][v] = (sb && ok[v]) ? __ldcg(reinterpret_cast<const uint4*>(sb + lr[v] * (D * 2) + c8[v] * 2))
+                                         : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            const int k = k0 + u;
+            if (k >= pieces) break;
+#pragma unroll
+            for (int v = 0; v < CH; ++v) {
+                float wt;
+                if (k < MERGE_MW) {
+                    wt = pw[k][lr[v]];
+                } else {
+                    const float2 ml = ml_of(k, lr[v]);
+                    wt = exp2f(ml.x - nz[lr[v]].x) * ml.y * nz[lr[v]].y;
+                }
+                const __half2* h = reinterpret_cast<const __half2*>(&xv[u][v]);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 f2 = __half22float2(h[q]);
+                    acc[v][2 * q] += wt * f2.x;
+                    acc[v][2 * q + 1] += wt * f2.y;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int v = 0; v < CH; ++v) {
+        if (!ok[v]) continue;
+        const int nl = lr[v] / p.G, hd = lr[v] % p.G;
+        const int nd = qt * p.npt + nl;
+        __nv_bfloat16* dst = p.out + (((int64_t)b * p.N + nd) * p.Hq + g * p.G + hd) * D + c8[v];
+        uint4 o;
+        o.x = pack_bf16x2(acc[v][0], acc[v][1]);
+        o.y = pack_bf16x2(acc[v][2], acc[v][3]);
+        o.z = pack_bf16x2(acc[v][4], acc[v][5]);
+        o.w = pack_bf16x2(acc[v][6], acc[v][7]);
+        *reinterpret_cast<uint4*>(dst) = o;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 int resident_clusters_tc(int cs) {
     static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
@@ -747,7 +1182,7 @@ int resident_clusters_tc(int cs) {
     cfg.attrs = &at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -762,10 +1197,39 @@ bool attn_tc_applicable(int N, int Hq, int Hkv, int d) {
     return d == D && G <= 128 && N * G > 64;
 }
 
+namespace {
+constexpr size_t kSchedBytes = 256;  // group counter and exit counter, padded
+
+int device_sms() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            sms = n;
+        else
+            cudaGetLastError();
+    }
+    return sms;
+}
+}  // namespace
+
+// Workspace: scheduler counters (zero between calls), then two partial-result
+// slots per CTA of a balanced-split grid (at most one CTA per SM).
+size_t attn_tc_zeroed_prefix(int B, int N, int Hq, int Hkv) {
+    (void)B; (void)N; (void)Hq; (void)Hkv;
+    return kSchedBytes;
+}
+size_t attn_tc_workspace(int B, int N, int Hq, int Hkv) {
+    return attn_tc_zeroed_prefix(B, N, Hq, Hkv) + (size_t)2 * device_sms() * SLOT_BYTES;
+}
+
 tv_status launch_attn_tc(const AttnArgs& a) {
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES) != cudaSuccess)
             return TV_ERR_CUDA;
         attr_set = true;
@@ -799,6 +1263,33 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     if (groups >= (1LL << 30)) return TV_ERR_UNSUPPORTED;
     prm.groups = (int)groups;
     prm.scale_log2 = a.scale * LOG2E;
+    // Balanced split when the groups are too few to give every SM one (whole
+    // groups would leave SMs idle) but not so few that clusters split them
+    // better, the workspace holds the partial results and the sequence count
+    // fits the in-kernel prefix sum.  Otherwise groups go to clusters
+    // dynamically, longest first.
+    {
+        const int ncta = resident_clusters_tc(1);
+        const int lanes = ncta / prm.QT;
+        const size_t zeroed = attn_tc_zeroed_prefix(a.B, a.N, a.Hq, a.Hkv);
+        const size_t need = zeroed + (size_t)2 * lanes * prm.QT * SLOT_BYTES;
+        const char* env = getenv("TV_SPLIT");
+        const bool want = env ? (env[0] != '0') : (groups < ncta && 2 * groups >= ncta);
+        if (want && lanes >= 1 && a.B <= LPT_MAX && a.ws_bytes >= need) {
+            prm.lanes = lanes;
+            const char* c0e = getenv("TV_SPLIT_C0");
+            prm.c0 = c0e ? std::max(0, atoi(c0e)) : SPLIT_C0;
+            prm.part = static_cast<uint8_t*>(a.ws) + zeroed;
+            LaunchCfg lc(dim3((unsigned)(lanes * prm.QT)), dim3(THREADS), SMEM_BYTES, a.stream, 1u);
+            if (cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel<true>, qm, km, vm, prm) != cudaSuccess)
+                return TV_ERR_CUDA;
+            if (lanes < 2) return TV_OK;  // one run: nothing is cut
+            LaunchCfg lm(dim3((unsigned)((lanes - 1) * prm.QT)), dim3(MERGE_THREADS), 0, a.stream, 1u);
+            return cudaLaunchKernelEx(&lm.cfg, attn_split_merge_kernel, prm) == cudaSuccess
+                       ? TV_OK
+                       : TV_ERR_CUDA;
+        }
+    }
     // cluster size: minimise rounds x (tiles per CTA + one tile of merge cost)
     const int64_t tiles_max = ((int64_t)a.max_blocks * a.bs + KT - 1) / KT;
     int best_cs = 1, best_ncl = 0;
@@ -819,7 +1310,7 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     const int clusters = (int)std::min<int64_t>(best_ncl, groups);
     LaunchCfg lc(dim3((unsigned)(clusters * best_cs)), dim3(THREADS), SMEM_BYTES, a.stream,
                  (unsigned)best_cs);
-    return cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel, qm, km, vm, prm) == cudaSuccess
+    return cudaLaunchKernelEx(&lc.cfg, attn_tc_kernel<false>, qm, km, vm, prm) == cudaSuccess
                ? TV_OK
                : TV_ERR_CUDA;
 }

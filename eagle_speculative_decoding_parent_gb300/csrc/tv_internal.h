@@ -91,6 +91,10 @@ size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks,
 // tensor-core (tcgen05) variant for row tiles wider than 64 rows; same workspace
 bool attn_tc_applicable(int N, int Hq, int Hkv, int d);
 tv_status launch_attn_tc(const AttnArgs& a);
+// its workspace (balanced split: counters and partial results) and the leading
+// bytes of it that must be zero when a call starts
+size_t attn_tc_workspace(int B, int N, int Hq, int Hkv);
+size_t attn_tc_zeroed_prefix(int B, int N, int Hq, int Hkv);
 // Leading bytes of that workspace that must be zero when a call starts.
 size_t attn_bf16_workspace_zeroed_prefix(int B, int N, int Hq, int Hkv, int d, int max_blocks,
                                          int bs);

@@ -116,12 +116,17 @@ tv_status tree_mask_build(const int32_t* parents, int B, int N, uint64_t* mask,
  * TV_ERR_OUT_OF_RANGE and zero outputs.  Positions beyond P_b + N - 1 in the
  * last block are never read into the result (they may hold anything, NaN
  * included).
- * workspace: device scratch of at least tree_verify_attention_workspace()
- * bytes, 256-byte aligned.  Its leading words are per-(sequence, kv head,
- * row tile) arrival counters that must be zero before the first call (zero
- * the whole buffer once); every call that completes leaves them at zero
- * again.  The rest holds split-KV partial results (softmax max, sum and
- * unnormalised output per key chunk).
+ * workspace: device scratch of tree_verify_attention_workspace() bytes,
+ * 256-byte aligned.  Its leading bytes are scheduler counters and
+ * per-(sequence, kv head, row tile) arrival counters that must be zero
+ * before the first call (zero the whole buffer once); every call that
+ * completes leaves them at zero again.  The rest holds split-KV partial
+ * results (per row: softmax max and sum, normalised output) of the
+ * balanced schedule, which gives every SM the same number of key tiles.
+ * A smaller workspace of at least 256 bytes is accepted and selects a
+ * schedule without partial results in global memory (groups of sequences
+ * handed to clusters of SMs); below 256 bytes the call returns
+ * TV_ERR_WORKSPACE.
  * ------------------------------------------------------------------------ */
 size_t tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
                                        int max_blocks_per_seq, int block_size, tv_dtype dt);
@@ -240,7 +245,7 @@ tv_status kv_compact(void* k_cache, void* v_cache, int num_layers, int64_t layer
  *   streams, or concurrent host threads) race on the array and must not be
  *   issued.
  * ------------------------------------------------------------------------ */
-#define TV_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+#define TV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 size_t tree_verify_attention_noalloc_capacity(void);
 

@@ -70,7 +70,9 @@ def test_mask_host_errors(tv):
 
 # ------------------------------------------------------------------ attention
 
-def run_attention(tv, w, mask_np=None, scale=0.0):
+def run_attention(tv, w, mask_np=None, scale=0.0, ws_bytes=None):
+    """ws_bytes: workspace size (default: the size the library asks for; 256
+    selects the schedule without partial results in global memory)."""
     spec = w["spec"]
     d = to_device(w)
     B, N = w["parents"].shape
@@ -79,6 +81,8 @@ def run_attention(tv, w, mask_np=None, scale=0.0):
     status = torch.full((B,), -9, dtype=torch.int32, device="cuda")
     ws = tv.tree_verify_attention_workspace(B, N, spec.Hq, spec.Hkv, spec.d,
                                             w["block_table"].shape[1], spec.bs, d["q"].dtype)
+    if ws_bytes is not None:
+        ws = ws_bytes
     wsb = torch.zeros(max(ws, 256), dtype=torch.uint8, device="cuda")
     tv.tree_verify_attention(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
                              d["prefix_lens"], mask, out, status, wsb, scale=scale)
@@ -142,6 +146,54 @@ def test_attention_bf16_small(tv, orc, case):
     # arrival counters are left at zero for the next call
     got2, _, _ = run_attention(tv, w)
     assert np.array_equal(got, got2)
+
+
+@pytest.mark.parametrize("case", [
+    # tensor-core row tiles (M > 64) under both schedules
+    (26, 32, 8, 128, 16, 1, 1500, 4),    # M = 104
+    (60, 32, 8, 128, 16, 2000, 2100, 1), # M = 240, one sequence over many SMs
+    (63, 28, 4, 128, 16, 700, 1000, 2),  # M = 441
+    (20, 16, 4, 128, 16, 0, 5000, 9),    # M = 80, very uneven prefixes
+])
+@pytest.mark.parametrize("schedule", ["balanced", "clusters", "clusters-small-ws"])
+def test_attention_tc_schedules(tv, orc, case, schedule, monkeypatch):
+    """The balanced split (forced on, whatever the group count) and the cluster
+    schedule (forced, or chosen because the workspace is too small for partial
+    results) give the same attention."""
+    monkeypatch.setenv("TV_SPLIT", "0" if schedule == "clusters" else "1")
+    ws_bytes = 256 if schedule == "clusters-small-ws" else None
+    N, Hq, Hkv, d, bs, plo, phi, B = case
+    spec = W.Spec("sched", B=B, P_lo=plo, P_hi=phi, Hq=Hq, Hkv=Hkv, d=d, V=16, N=N,
+                  tree="random", depth=8, branch=4, bs=bs, seed=7 + sum(case))
+    w = with_mask(orc, small(spec))
+    got, st, _ = run_attention(tv, w, ws_bytes=ws_bytes)
+    ref, rst = oracle_attention(orc, w)
+    assert (st == 0).all() and (rst == 0).all()
+    assert_close_bf16(got.reshape(ref.shape), ref)
+    got2, _, _ = run_attention(tv, w, ws_bytes=ws_bytes)
+    assert np.array_equal(got, got2)
+
+
+def test_attention_tc_balanced_flags_bad_sequences(tv, orc, monkeypatch):
+    """Balanced schedule: a sequence with a block id outside the cache and one
+    with a negative prefix length get status 3 and zero outputs; the others,
+    whose groups are cut into pieces around them, stay exact."""
+    monkeypatch.setenv("TV_SPLIT", "1")
+    spec = W.Spec("badtc", B=5, P_lo=600, P_hi=3000, Hq=32, Hkv=8, d=128, V=16, N=26,
+                  tree="random", depth=6, branch=4, seed=21)
+    w = with_mask(orc, small(spec))
+    ref, _ = oracle_attention(orc, w)
+    w["block_table"] = w["block_table"].copy()
+    w["block_table"][1, 3] = w["k_cache"].shape[0] + 1
+    w["prefix_lens"] = w["prefix_lens"].copy()
+    w["prefix_lens"][3] = -5
+    got, st, _ = run_attention(tv, w)
+    assert list(st) == [0, orc.OUT_OF_RANGE, 0, orc.OUT_OF_RANGE, 0]
+    g = got.reshape(5, spec.N, spec.Hq, spec.d)
+    r = ref.reshape(5, spec.N, spec.Hq, spec.d)
+    assert (g[1] == 0).all() and (g[3] == 0).all()
+    for b in (0, 2, 4):
+        assert_close_bf16(g[b], r[b])
 
 
 FULL = ["llama3_8b_tree60", "llama3_8b_b32_tree26", "llama3_8b_b128_chain5",
