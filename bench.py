@@ -277,6 +277,11 @@ def run_ours(args):
     dtype = d["q"].dtype
     step = VerifyStep(B=B, N=N, Hq=s.Hq, Hkv=s.Hkv, d=s.d, max_blocks=w["block_table"].shape[1],
                       bs=s.bs, dtype=dtype, max_path=mp, V=s.V, mode=mode)
+    # kernels per step: mask, accept and compaction launch one each; attention one,
+    # or two when it takes the balanced schedule (a merge kernel follows)
+    attn_kernels = tv.tree_verify_attention_kernels(
+        B, N, s.Hq, s.Hkv, s.d, w["block_table"].shape[1], s.bs, dtype,
+        step.workspace.numel())
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
@@ -428,7 +433,7 @@ def run_ours(args):
                 "cpu_baseline": cpu,
                 "e2e": {"value": world * B * N / (e2e_ms * 1e-3), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": 4 * args.steps,
+                "gpu_launches": (3 + attn_kernels) * args.steps,
                 "clocks": clocks,
                 "kernel_ms": {n: float(m) for n, m in zip(names, mean_ms)},
                 "attention_kv_gbs": attn_gbs,

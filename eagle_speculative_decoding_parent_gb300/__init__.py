@@ -23,7 +23,8 @@ from . import _build
 __all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTED",
            "TV_ERR_TIMEOUT", "TV_ERR_BAD_VALUES", "TV_F32", "TV_BF16", "GREEDY", "STOCHASTIC",
            "TreeVerifyError", "library_path", "status_string", "tree_mask_build",
-           "tree_verify_attention_workspace", "tree_verify_attention",
+           "tree_verify_attention_workspace", "tree_verify_attention_kernels",
+           "tree_verify_attention",
            "tree_verify_attention_noalloc", "tree_verify_attention_noalloc_capacity",
            "tree_accept_workspace",
            "tree_accept", "kv_compact"]
@@ -63,6 +64,7 @@ _status_string = _sig("tv_status_string", ctypes.c_char_p, [_i])
 _abi = _sig("tv_abi_version", _i, [])
 _mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p])
 _attn_ws = _sig("tree_verify_attention_workspace", _sz, [_i, _i, _i, _i, _i, _i, _i, _i])
+_attn_nk = _sig("tree_verify_attention_kernels", _i, [_i, _i, _i, _i, _i, _i, _i, _i, _sz])
 _attn = _sig("tree_verify_attention", _i,
              [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p])
 _attn_na = _sig("tree_verify_attention_noalloc", _i,
@@ -130,6 +132,13 @@ def tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_blocks_per_seq, block_
                                     dtype=torch.bfloat16) -> int:
     dt = TV_BF16 if dtype == torch.bfloat16 else TV_F32
     return int(_attn_ws(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size, dt))
+
+
+def tree_verify_attention_kernels(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size,
+                                  dtype=torch.bfloat16, workspace_bytes: int = 0) -> int:
+    """Kernels one tree_verify_attention call launches (launch accounting)."""
+    dt = TV_BF16 if dtype == torch.bfloat16 else TV_F32
+    return int(_attn_nk(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size, dt, workspace_bytes))
 
 
 def tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, mask, out, status,

@@ -75,6 +75,19 @@ size_t tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
     return attn_bf16_workspace(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size);
 }
 
+int tree_verify_attention_kernels(int B, int N, int Hq, int Hkv, int d, int max_blocks_per_seq,
+                                  int block_size, tv_dtype dt, size_t workspace_bytes) {
+    if (dt != TV_F32 && dt != TV_BF16) return -1;
+    if (B < 0 || N < 1 || N > 64 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 ||
+        block_size < 1)
+        return -1;
+    if (!attn_shape_ok(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size, dt)) return -1;
+    if (B == 0) return 0;
+    if (dt == TV_BF16 && attn_tc_applicable(N, Hq, Hkv, d))
+        return attn_tc_kernels(B, N, Hq, Hkv, workspace_bytes);
+    return 1;
+}
+
 tv_status tree_verify_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks_per_seq,
                                 const int32_t* prefix_lens, const uint64_t* mask, int B, int N,

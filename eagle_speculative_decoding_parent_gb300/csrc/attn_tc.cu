@@ -1224,6 +1224,29 @@ size_t attn_tc_workspace(int B, int N, int Hq, int Hkv) {
     return attn_tc_zeroed_prefix(B, N, Hq, Hkv) + (size_t)2 * device_sms() * SLOT_BYTES;
 }
 
+// The schedule a call takes: the balanced split (lanes CTAs per row tile) or 0
+// for clusters.  Balanced split when the groups are too few to give every SM
+// one (whole groups would leave SMs idle) but not so few that clusters split
+// them better, the workspace holds the partial results and the sequence count
+// fits the in-kernel prefix sum.  Otherwise groups go to clusters dynamically,
+// longest first.
+int tc_split_lanes(int B, int N, int Hq, int Hkv, size_t ws_bytes) {
+    const int npt = 128 / (Hq / Hkv);
+    const int QT = (N + npt - 1) / npt;
+    const int64_t groups = (int64_t)B * Hkv * QT;
+    const int ncta = resident_clusters_tc(1);
+    const int lanes = ncta / QT;
+    const size_t need = attn_tc_zeroed_prefix(B, N, Hq, Hkv) + (size_t)2 * lanes * QT * SLOT_BYTES;
+    const char* env = getenv("TV_SPLIT");
+    const bool want = env ? (env[0] != '0') : (groups < ncta && 2 * groups >= ncta);
+    return (want && lanes >= 1 && B <= LPT_MAX && ws_bytes >= need) ? lanes : 0;
+}
+
+int attn_tc_kernels(int B, int N, int Hq, int Hkv, size_t ws_bytes) {
+    const int lanes = tc_split_lanes(B, N, Hq, Hkv, ws_bytes);
+    return lanes >= 2 ? 2 : 1;
+}
+
 tv_status launch_attn_tc(const AttnArgs& a) {
     static bool attr_set = false;
     if (!attr_set) {
@@ -1263,19 +1286,10 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     if (groups >= (1LL << 30)) return TV_ERR_UNSUPPORTED;
     prm.groups = (int)groups;
     prm.scale_log2 = a.scale * LOG2E;
-    // Balanced split when the groups are too few to give every SM one (whole
-    // groups would leave SMs idle) but not so few that clusters split them
-    // better, the workspace holds the partial results and the sequence count
-    // fits the in-kernel prefix sum.  Otherwise groups go to clusters
-    // dynamically, longest first.
     {
-        const int ncta = resident_clusters_tc(1);
-        const int lanes = ncta / prm.QT;
-        const size_t zeroed = attn_tc_zeroed_prefix(a.B, a.N, a.Hq, a.Hkv);
-        const size_t need = zeroed + (size_t)2 * lanes * prm.QT * SLOT_BYTES;
-        const char* env = getenv("TV_SPLIT");
-        const bool want = env ? (env[0] != '0') : (groups < ncta && 2 * groups >= ncta);
-        if (want && lanes >= 1 && a.B <= LPT_MAX && a.ws_bytes >= need) {
+        const int lanes = tc_split_lanes(a.B, a.N, a.Hq, a.Hkv, a.ws_bytes);
+        if (lanes > 0) {
+            const size_t zeroed = attn_tc_zeroed_prefix(a.B, a.N, a.Hq, a.Hkv);
             prm.lanes = lanes;
             const char* c0e = getenv("TV_SPLIT_C0");
             prm.c0 = c0e ? std::max(0, atoi(c0e)) : SPLIT_C0;

@@ -95,6 +95,8 @@ tv_status launch_attn_tc(const AttnArgs& a);
 // bytes of it that must be zero when a call starts
 size_t attn_tc_workspace(int B, int N, int Hq, int Hkv);
 size_t attn_tc_zeroed_prefix(int B, int N, int Hq, int Hkv);
+// kernels one tensor-core attention call launches with this workspace size
+int attn_tc_kernels(int B, int N, int Hq, int Hkv, size_t ws_bytes);
 // Leading bytes of that workspace that must be zero when a call starts.
 size_t attn_bf16_workspace_zeroed_prefix(int B, int N, int Hq, int Hkv, int d, int max_blocks,
                                          int bs);

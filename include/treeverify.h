@@ -131,6 +131,13 @@ tv_status tree_mask_build(const int32_t* parents, int B, int N, uint64_t* mask,
 size_t tree_verify_attention_workspace(int B, int N, int Hq, int Hkv, int d,
                                        int max_blocks_per_seq, int block_size, tv_dtype dt);
 
+/* Kernels one tree_verify_attention call with these sizes and this workspace
+ * size launches on the current device (launch accounting: the balanced
+ * schedule adds a merge kernel); 0 when B = 0, -1 for arguments the call
+ * rejects before launching. */
+int tree_verify_attention_kernels(int B, int N, int Hq, int Hkv, int d, int max_blocks_per_seq,
+                                  int block_size, tv_dtype dt, size_t workspace_bytes);
+
 tv_status tree_verify_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks_per_seq,
                                 const int32_t* prefix_lens, const uint64_t* mask, int B, int N,

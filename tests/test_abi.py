@@ -72,6 +72,12 @@ def test_host_argument_checks_need_no_gpu(lib):
     # Hq not a multiple of Hkv -> invalid
     assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, 6, 4, 128, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
              None) == 1
+    # kernel count query: rejected shapes -> -1, empty batch -> 0 (no device needed)
+    k = lib.tree_verify_attention_kernels
+    k.argtypes = [ctypes.c_int] * 8 + [ctypes.c_size_t]
+    assert k(1, 4, 6, 4, 128, 10, 16, 1, 0) == -1     # Hq not a multiple of Hkv
+    assert k(1, 65, 8, 2, 128, 10, 16, 1, 0) == -1    # more than 64 nodes
+    assert k(0, 4, 8, 2, 128, 10, 16, 1, 0) == 0
     # kv_compact: rows that are not a multiple of 16 bytes -> unsupported
     c = lib.kv_compact
     c.argtypes = [p, p, ctypes.c_int, ctypes.c_int64, p, ctypes.c_int, p, p, p] + \

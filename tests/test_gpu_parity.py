@@ -196,6 +196,18 @@ def test_attention_tc_balanced_flags_bad_sequences(tv, orc, monkeypatch):
         assert_close_bf16(g[b], r[b])
 
 
+def test_attention_kernel_count(tv):
+    """The launch count the library reports: the balanced schedule (row tiles
+    too few for the SMs, full workspace) adds a merge kernel."""
+    bf = torch.bfloat16
+    full = tv.tree_verify_attention_workspace(8, 63, 28, 4, 128, 2100, 16, bf)
+    assert tv.tree_verify_attention_kernels(8, 63, 28, 4, 128, 2100, 16, bf, full) == 2
+    assert tv.tree_verify_attention_kernels(8, 63, 28, 4, 128, 2100, 16, bf, 256) == 1
+    assert tv.tree_verify_attention_kernels(1, 60, 32, 8, 128, 200, 16, bf, 1 << 30) == 1
+    assert tv.tree_verify_attention_kernels(128, 6, 32, 8, 128, 300, 16, bf, 1 << 30) == 1
+    assert tv.tree_verify_attention_kernels(0, 6, 32, 8, 128, 300, 16, bf, 0) == 0
+
+
 FULL = ["llama3_8b_tree60", "llama3_8b_b32_tree26", "llama3_8b_b128_chain5",
         "qwen2_7b_32k_tree63"]
 
