@@ -359,7 +359,7 @@ def run_ours(args):
     peak = peaks["hbm_gbs"] if peaks else 6800.0
     alg = {1: attn_bytes(w), 2: accept_bytes(w, acc_len)}.get(dom)
     G = s.Hq // s.Hkv
-    tc = bf and s.d == 128 and G <= 128 and N * G > 64  # the tensor-memory attention kernel
+    tc = bf and s.d == 128 and G <= 128  # the tensor-memory attention kernel
     files = {0: "tree_mask.cu", 1: ("attn_tc.cu" if tc else "attn_bf16.cu") if bf else "attn_f32.cu",
              2: "accept.cu", 3: "kv_compact.cu"}
     if alg is None:

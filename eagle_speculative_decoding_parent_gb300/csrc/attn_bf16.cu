@@ -1,4 +1,5 @@
-// tree_verify_attention, bfloat16 path.
+// tree_verify_attention, bfloat16 path on warp-level MMA: head size 64 (head
+// size 128 runs on the tensor-memory kernel, attn_tc.cu).
 //
 // Work decomposition
 //   All query heads of one KV group times all tree nodes form one packed row

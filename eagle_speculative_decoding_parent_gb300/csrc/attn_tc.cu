@@ -1,7 +1,7 @@
 // tree_verify_attention, bfloat16 path on the 5th-generation tensor cores.
 //
-// Used when the packed row tile is a real dense contraction (more than 64
-// rows).  A group is (sequence, kv head, row tile).  Two schedules:
+// Used for head size 128 (the warp-MMA kernel serves head size 64).  A group
+// is (sequence, kv head, row tile).  Two schedules:
 //   balanced split (when the caller's workspace holds the partial results):
 //            the grid is QT CTAs (one per row tile) times `lanes`; the key
 //            tiles of all (sequence, kv head) pairs, laid end to end, are cut
@@ -1192,9 +1192,15 @@ int resident_clusters_tc(int cs) {
 
 }  // namespace
 
+// Every head-size-128 shape.  Even a row tile of a few dozen rows (a chain of
+// 6 nodes x 4 heads) is faster here, padded to 128 rows, than on the warp-MMA
+// kernel: the tensor cores leave the tile loop bound by the K/V stream, while
+// the warp-MMA kernel's per-tile chain of dependent steps bounds it well below
+// that (llama3-8B b128 chain5: 274 against 331 us).
 bool attn_tc_applicable(int N, int Hq, int Hkv, int d) {
+    (void)N;
     const int G = Hq / Hkv;
-    return d == D && G <= 128 && N * G > 64;
+    return d == D && G <= 128;
 }
 
 namespace {

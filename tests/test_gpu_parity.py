@@ -124,14 +124,17 @@ def test_attention_f32_tiny_workload(tv, orc):
 
 @pytest.mark.parametrize("case", [
     # (N, Hq, Hkv, d, bs, P_lo, P_hi, B)  -> packed rows M = N * Hq / Hkv
-    (4, 8, 2, 128, 16, 0, 300, 3),       # M = 16   (1 x 8 warps)
-    (6, 32, 8, 128, 16, 900, 2100, 5),   # M = 24   (2 x 4)  chain-like
-    (13, 8, 2, 128, 32, 64, 700, 4),     # M = 52   (4 x 2), block size 32
-    (26, 32, 8, 128, 16, 1, 1500, 4),    # M = 104  (8 x 1)
+    # head size 128: tensor-memory kernel (row tiles padded to 128 rows)
+    (4, 8, 2, 128, 16, 0, 300, 3),       # M = 16
+    (6, 32, 8, 128, 16, 900, 2100, 5),   # M = 24   chain-like
+    (13, 8, 2, 128, 32, 64, 700, 4),     # M = 52   block size 32
+    (26, 32, 8, 128, 16, 1, 1500, 4),    # M = 104
     (60, 32, 8, 128, 16, 2000, 2100, 1), # M = 240  (two row tiles)
     (63, 28, 4, 128, 16, 700, 1000, 2),  # M = 441  (four row tiles)
-    (7, 2, 1, 64, 16, 0, 130, 3),        # head size 64
-    (33, 16, 4, 64, 16, 50, 333, 3),     # head size 64, M = 132
+    # head size 64: warp-MMA kernel (row warps x key groups)
+    (7, 2, 1, 64, 16, 0, 130, 3),        # M = 14   (1 x 8 warps)
+    (33, 16, 4, 64, 16, 50, 333, 3),     # M = 132  (several row tiles)
+    (6, 32, 8, 64, 16, 900, 2100, 5),    # M = 24   (2 x 4)  chain-like
     (1, 4, 4, 128, 16, 0, 65, 4),        # root only, empty prefix possible
 ])
 def test_attention_bf16_small(tv, orc, case):
