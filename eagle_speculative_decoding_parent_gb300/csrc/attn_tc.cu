@@ -1166,10 +1166,28 @@ attn_split_merge_kernel(Params p) {
 }
 
 // ---------------------------------------------------------------- host side
+// Both instantiations may use SMEM_BYTES of dynamic shared memory; set before
+// any launch or occupancy query (a query without it finds no room).
+bool tc_attrs_set() {
+    static bool done = false;
+    if (!done) {
+        if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        done = true;
+    }
+    return true;
+}
+
 int resident_clusters_tc(int cs) {
     static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
     if (cs < 1 || cs > 8) return 0;
     if (cache[cs] >= 0) return cache[cs];
+    if (!tc_attrs_set()) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs);
     cfg.blockDim = dim3(THREADS);
@@ -1184,7 +1202,7 @@ int resident_clusters_tc(int cs) {
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel<false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
-        n = 0;
+        return 0;  // not cached: a later query may succeed
     }
     cache[cs] = n;
     return n;
@@ -1254,15 +1272,7 @@ int attn_tc_kernels(int B, int N, int Hq, int Hkv, size_t ws_bytes) {
 }
 
 tv_status launch_attn_tc(const AttnArgs& a) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess ||
-            cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
-            return TV_ERR_CUDA;
-        attr_set = true;
-    }
+    if (!tc_attrs_set()) return TV_ERR_CUDA;
     const int G = a.Hq / a.Hkv;
     const int npt = 128 / G;
     const int64_t rows = (int64_t)a.num_blocks * a.Hkv * a.bs;
