@@ -157,6 +157,8 @@ def test_attention_bf16_small(tv, orc, case):
     (60, 32, 8, 128, 16, 2000, 2100, 1), # M = 240, one sequence over many SMs
     (63, 28, 4, 128, 16, 700, 1000, 2),  # M = 441
     (20, 16, 4, 128, 16, 0, 5000, 9),    # M = 80, very uneven prefixes
+    (20, 16, 4, 128, 16, 4000, 5000, 1), # one sequence cut into ~38 pieces per group
+    (2, 64, 64, 128, 16, 0, 60, 256),    # G = 1: 16k one-tile groups, ~100 pieces per run
 ])
 @pytest.mark.parametrize("schedule", ["balanced", "clusters", "clusters-small-ws"])
 def test_attention_tc_schedules(tv, orc, case, schedule, monkeypatch):
