@@ -85,13 +85,13 @@ constexpr int NUM_BARS = 2 * STAGES + 2 + 2 * 4 + 2 + 2 * GQ + 2;
 constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
 constexpr int OFF_LPT = OFF_MISC + 64;                 // sequence order: lens, order
 constexpr int OFF_CUM = OFF_LPT + 2 * LPT_MAX * 4;     // balanced split: int64 [LPT_MAX + 1]
-constexpr int OFF_GQT = OFF_CUM + (LPT_MAX + 1) * 8 + 8;  // key-tile range per queue slot [GQ][2]
+constexpr int OFF_GQ4 = OFF_CUM + (LPT_MAX + 1) * 8 + 8;  // queue slots [GQ] x (word, first tile, end tile, -)
 constexpr int MAXI = 64;                               // balanced split: pieces listed up front
-constexpr int OFF_ITEMS = OFF_GQT + GQ * 8;            // [MAXI] x (word, first tile, end tile, bad)
+constexpr int OFF_ITEMS = OFF_GQ4 + GQ * 16;           // [MAXI] x (word, first tile, end tile, bad)
 constexpr int OFF_NITEMS = OFF_ITEMS + MAXI * 16;
 constexpr int SMEM_BYTES = OFF_NITEMS + 16 + 1024;     // + alignment slack
 static_assert(OFF_CUM % 8 == 0, "int64 prefix sums");
-static_assert(OFF_ITEMS % 16 == 0, "int4 items");
+static_assert(OFF_ITEMS % 16 == 0 && OFF_GQ4 % 16 == 0, "int4 slots");
 // Balanced split: cost of starting a piece (Q tile, pipeline fill and drain,
 // epilogue), in key-tile times.
 constexpr int SPLIT_C0 = 4;
@@ -255,10 +255,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* xready = gq_empty + GQ;
     uint64_t* xfree = xready + 1;
     int* misc = reinterpret_cast<int*>(smem + OFF_MISC);
-    int* gq = misc;                           // [GQ]
+    // queue slot: the group word (stored into every cluster rank) and, for the
+    // balanced split, the piece's key tiles; read with one 16-byte load
+    int4* gq4 = reinterpret_cast<int4*>(smem + OFF_GQ4);
     uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(misc + GQ);
     int* flags = misc + GQ + 1;               // [0] abort
-    int* gqt = reinterpret_cast<int*>(smem + OFF_GQT);  // [GQ][2] key tiles of the item
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank(), cs = cluster_size();
@@ -473,21 +474,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
             }
             if (lane == 0) {
-                gqt[2 * slot] = tlo;  // balanced split only: no cluster peers
-                gqt[2 * slot + 1] = thi;
+                gq4[slot].y = tlo;  // balanced split only: no cluster peers
+                gq4[slot].z = thi;
                 for (uint32_t r = 0; r < cs; ++r) {
-                    remote_st_u32(&gq[slot], r, word);
+                    remote_st_u32(&gq4[slot].x, r, word);
                     remote_arrive(&gq_full[slot], r);
                 }
             }
         }
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&gq_full[slot], (k / GQ) & 1u));
+        const int4 v = lds_v4_volatile(&gq4[slot]);
         Item it;
-        it.word = got ? *(volatile int*)&gq[slot] : p.groups;
-        it.t_lo = *(volatile int*)&gqt[2 * slot];
-        it.t_hi = *(volatile int*)&gqt[2 * slot + 1];
+        it.word = got ? v.x : p.groups;
+        it.t_lo = v.y;
+        it.t_hi = v.z;
         __syncwarp();
-        if (lane == 0) remote_arrive(&gq_empty[slot], 0);
+        // "slot read": no release needed, and a release here would wait for the
+        // softmax warps' output stores of the previous group
+        if (lane == 0) remote_arrive_relaxed_after(&gq_empty[slot], 0, got ? v.x : 0);
         return it;
     };
 

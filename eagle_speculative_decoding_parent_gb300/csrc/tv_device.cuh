@@ -269,6 +269,24 @@ __device__ __forceinline__ void remote_arrive(uint64_t* bar, uint32_t rank) {
                      map_rank(bar, rank))
                  : "memory");
 }
+// Arrive on `bar` of cluster rank `rank` without release semantics (a release
+// waits for every earlier global store of the thread to be acknowledged).  The
+// barrier address is made to depend on `dep`, a non-negative value the thread
+// loaded just before, so the arrive cannot be performed before that load:
+// enough for a consumer that only signals "slot read".
+__device__ __forceinline__ void remote_arrive_relaxed_after(uint64_t* bar, uint32_t rank, int dep) {
+    const uint32_t a = map_rank(bar, rank) + (((uint32_t)dep >> 31) << 3);  // + 0 for dep >= 0
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(a) : "memory");
+}
+// 16-byte shared-memory load that is always performed (never cached in registers).
+__device__ __forceinline__ int4 lds_v4_volatile(const int4* p) {
+    int4 v;
+    asm volatile("ld.volatile.shared.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p))
+                 : "memory");
+    return v;
+}
 __device__ __forceinline__ void remote_st_u32(int* p, uint32_t rank, int v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(map_rank(p, rank)), "r"(v) : "memory");
 }
