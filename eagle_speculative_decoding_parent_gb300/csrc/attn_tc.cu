@@ -1042,7 +1042,12 @@ attn_split_merge_kernel(Params p) {
     const int64_t L = min((int64_t)p.lanes, U);
     const int64_t l = blockIdx.x / p.QT + 1;
     const int qt = (int)(blockIdx.x % p.QT);
-    if (l >= L) return;
+    // every path waits for the attention grid before it ends: under programmatic
+    // dependent launch the next kernel waits only for this grid
+    if (l >= L) {
+        pdl_wait();
+        return;
+    }
     const int64_t x = run_start(l, U, L);
     int b = 0, hi = p.B;  // cum[b] <= x < cum[hi]
     while (hi - b > 1) {
@@ -1053,7 +1058,10 @@ attn_split_merge_kernel(Params p) {
     const int64_t w = (cum[b + 1] - cum[b]) / p.Hkv;
     const int64_t g0 = x - (x - cum[b]) % w;
     const int64_t F = g0 + p.c0, tb = w - p.c0;  // the group's first tile unit, tiles
-    if (x <= F || run_start(l - 1, U, L) > F) return;  // not cut here first
+    if (x <= F || run_start(l - 1, U, L) > F) {  // not cut here first
+        pdl_wait();
+        return;
+    }
     const int g = (int)((g0 - cum[b]) / w);
     const int64_t l1 = run_owner(F + tb - 1, U, L);
     const int pieces = (int)(l1 - (l - 1) + 1);
