@@ -2,24 +2,26 @@
 //
 // Used for head size 128 (the warp-MMA kernel serves head size 64).  A group
 // is (sequence, kv head, row tile).  Two schedules:
-//   balanced split (when the caller's workspace holds the partial results):
+//   balanced split (groups too few to give every SM one, but at least half
+//            as many, and the caller's workspace holds the partial results):
 //            the grid is QT CTAs (one per row tile) times `lanes`; the key
-//            tiles of all (sequence, kv head) pairs, laid end to end, are cut
-//            into `lanes` runs of equal length, so every CTA streams the same
-//            number of tiles.  A group cut by a run boundary leaves one partial
-//            result (running max, sum, normalised O) per run in global memory,
-//            and the last run to finish, seen from an arrival counter, merges
-//            them.
-//   clusters (otherwise): groups go dynamically to clusters of CS CTAs that
-//            split the group's keys and merge through distributed shared memory.
+//            tiles of all (sequence, kv head) pairs, laid end to end with a
+//            fixed cost per piece, are cut into `lanes` runs of equal length,
+//            so every CTA streams the same work.  A group cut by a run
+//            boundary leaves one partial result (running max, sum, normalised
+//            O) per run in global memory; a second kernel, launched under
+//            programmatic dependent launch, merges them.
+//   clusters (otherwise): groups go dynamically, longest first, to clusters of
+//            CS CTAs that split the group's keys and merge through distributed
+//            shared memory.
 // A row tile holds npt = floor(128 / G) whole nodes (all G query heads of the
 // kv head for each), rows r = node * G + head, so one TMA box loads it.
 //
 // CTA roles (256 threads, one CTA per SM)
 //   warp 0   producer of pages 0-1 of each 64-key K/V tile; warp 2 loads
-//            pages 2-3.  A 16-key page is
-//            two K boxes (one per 64-column half) and one V box holding both
-//            halves; the ring has 5 stages (4 when a cluster splits the group).
+//            pages 2-3.  A 16-key page is two K boxes (one per 64-column half)
+//            and one V box holding both halves; the ring has 5 stages (4 when a
+//            cluster splits the group).
 //            Warp 0 of rank 0 also hands out the work items; warp 2 allocates /
 //            frees 512 tensor-memory columns: S double buffer (2 x 64), O (128),
 //            P (2 x 32).
