@@ -149,6 +149,27 @@ def accept_stochastic(parents, tokens, p, q, seed, offset, max_path):
     return acc, path, out, status
 
 
+def accept_stochastic_tree(parents, tokens, p, q, seed, offset, max_path):
+    """The branching-tree rule applied to every sequence, chains included (the
+    public accept_stochastic takes the chain rule for chains) -> same outputs."""
+    lib = _load()
+    parents = _c(parents, np.int32)
+    tokens = _c(tokens, np.int32)
+    p = _c(p, np.float32)
+    q = _c(q, np.float32)
+    B, N, V = p.shape
+    acc = np.zeros(B, np.int32)
+    path = np.zeros((B, max_path), np.int32)
+    out = np.zeros((B, max_path), np.int32)
+    status = np.zeros(B, np.int32)
+    for b in range(B):
+        lib.orc_accept_stochastic_tree(
+            _p(parents[b]), _p(tokens[b]), _p(p[b]), _p(q[b]), I64(1), I64(N), I64(V),
+            ctypes.c_uint64(seed), ctypes.c_uint64(offset), I64(max_path), _p(acc[b:]),
+            _p(path[b]), _p(out[b]), _p(status[b:]), I64(b))
+    return acc, path, out, status
+
+
 def philox4x32_10(counter, key):
     """One Philox4x32-10 block: counter 4 x uint32, key 2 x uint32 -> 4 x uint32."""
     lib = _load()

@@ -33,10 +33,12 @@
  *   - greedy: argmax takes the lowest index on ties and NaN never wins;
  *     the accepted node is the deepest fully matching one, ties to the
  *     smallest id;
- *   - stochastic (chain only): Philox4x32-10 (Salmon et al., SC'11) keyed by
- *     the seed, counter (k, b, offset_lo, offset_hi); accept iff
- *     u24 * q < p * 2^24 exactly; residual max(0, p - q) sampled through an
- *     integer CDF with 2^-40 resolution; see orc_accept_stochastic.
+ *   - stochastic: Philox4x32-10 (Salmon et al., SC'11) keyed by the seed,
+ *     counter (k, b, offset_lo, offset_hi); accept iff u24 * q < p * 2^24
+ *     exactly; residual max(0, p - q) sampled through an integer CDF with
+ *     2^-40 resolution; on a branching tree the children of a node are tried
+ *     in node order with the residual carried in exact integer weights; see
+ *     orc_accept_stochastic and orc_accept_stochastic_tree.
  *
  * Parity pins live in tests/test_oracle_*.py.
  */
@@ -364,6 +366,125 @@ static int64_t orc_sample_weights(const uint64_t* w, int64_t V, uint32_t x) {
     return -1; /* unreachable: T < S */
 }
 
+/* Rejection sampling on a branching draft tree, generalising the chain rule
+ * (multi-candidate speculative sampling: the children of the current node are
+ * tried in node order, and after each rejection the target is replaced by
+ * the normalised residual max(0, p - q); [P4] 无损性保障 states only that the
+ * result follows the target distribution, so the rule is ours).  Node c >= 1
+ * carries token x_c drawn from q row c; p row c is the target for the token
+ * after node c.  Starting at the root (cur = 0):
+ *   - the first child c of cur is tested as in the chain: u24 = word0 >> 8 of
+ *     draw (b, c), accept iff u24 * q_c(x_c) < p_cur(x_c) * 2^24 (exact in
+ *     double);
+ *   - after a rejection the residual is kept as exact integer weights w_t with
+ *     sum S: after the first rejected child c, w_t = weight(max(0, p_cur,t -
+ *     q_c,t)) (one binary32 subtraction); after each further rejected child
+ *     c', w_t <- max(0, w_t - floor(weight(q_c',t) * S / 2^40)) with the S
+ *     before the update;
+ *   - a later child c' is accepted iff u24 * weight(q_c'(x)) * S < w_x * 2^64,
+ *     i.e. u24/2^24 * q_c'(x) < w_x / S in exact integers (the left product
+ *     u24 * weight < 2^64, times S is formed in 128 bits);
+ *   - accepted child: it becomes cur, and its children are tried next;
+ *   - every child rejected: the emitted token is drawn from the residual
+ *     weights with word1 of the last rejected child's draw; if the residual
+ *     sums to 0 (then no later child is tried) it is drawn from
+ *     weight(p_cur,t) with that word instead;
+ *   - cur has no children: the bonus token is drawn from weight(p_cur,t) with
+ *     word1 of draw (b, N) when cur is node N-1, else of draw (b, N + cur), so
+ *     that no draw is used twice.
+ * On a chain this is exactly orc_accept_stochastic.  Rows p, q, outputs and
+ * status for one sequence (the caller offsets them); b keys the draws. */
+int orc_accept_stochastic_tree(const int32_t* par, const int32_t* tok, const float* p,
+                               const float* q, int64_t one, int64_t N, int64_t V, uint64_t seed,
+                               uint64_t offset, int64_t max_path, int32_t* accept_len,
+                               int32_t* path, int32_t* out_tokens, int32_t* status, int64_t b) {
+    (void)one;
+    int st = orc_check_tree(par, N);
+    for (int64_t c = 1; st == ORC_OK && c < N; ++c)
+        if (tok[c] < 0 || tok[c] >= V) st = ORC_OUT_OF_RANGE;
+    if (st == ORC_OK && max_path < 1) st = ORC_OUT_OF_RANGE;
+    if (st != ORC_OK) {
+        status[0] = st;
+        orc_accept_fail(0, max_path, accept_len, path, out_tokens);
+        return 0;
+    }
+    uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * V);
+    int64_t cur = 0;
+    int64_t emitted = -1;
+    for (;;) {
+        int64_t last_rej = -1;
+        uint64_t S = 0;
+        int accepted = 0;
+        const float* pc = p + cur * V;
+        for (int64_t c = cur + 1; c < N; ++c) {
+            if (par[c] != cur) continue;
+            uint32_t dw[4];
+            orc_draw(seed, offset, b, c, dw);
+            const uint32_t u24 = dw[0] >> 8;
+            const int64_t x = tok[c];
+            const float* qc = q + c * V;
+            int acc;
+            if (last_rej < 0) {
+                acc = (double)u24 * (double)qc[x] < (double)pc[x] * 16777216.0;
+            } else {
+                const unsigned __int128 lhs =
+                    (unsigned __int128)((uint64_t)u24 * orc_weight(qc[x])) * S;
+                acc = lhs < ((unsigned __int128)w[x] << 64);
+            }
+            if (acc) {
+                cur = c;
+                accepted = 1;
+                break;
+            }
+            /* residual update */
+            if (last_rej < 0) {
+                S = 0;
+                for (int64_t t = 0; t < V; ++t) {
+                    const float r = pc[t] - qc[t];
+                    w[t] = orc_weight(r);
+                    S += w[t];
+                }
+            } else {
+                uint64_t S2 = 0;
+                for (int64_t t = 0; t < V; ++t) {
+                    const uint64_t d =
+                        (uint64_t)(((unsigned __int128)orc_weight(qc[t]) * S) >> 40);
+                    w[t] = w[t] > d ? w[t] - d : 0;
+                    S2 += w[t];
+                }
+                S = S2;
+            }
+            last_rej = c;
+            if (S == 0) break;
+        }
+        if (accepted) continue;
+        if (last_rej < 0) {
+            /* a leaf: bonus token from the target row */
+            uint32_t dw[4];
+            orc_draw(seed, offset, b, (cur == N - 1) ? N : N + cur, dw);
+            for (int64_t t = 0; t < V; ++t) w[t] = orc_weight(pc[t]);
+            emitted = orc_sample_weights(w, V, dw[1]);
+        } else {
+            uint32_t dw[4];
+            orc_draw(seed, offset, b, last_rej, dw);
+            if (S > 0) {
+                emitted = orc_sample_weights(w, V, dw[1]);
+            } else {
+                for (int64_t t = 0; t < V; ++t) w[t] = orc_weight(pc[t]);
+                emitted = orc_sample_weights(w, V, dw[1]);
+            }
+        }
+        break;
+    }
+    free(w);
+    if (emitted < 0) st = ORC_BAD_VALUES;
+    if (st == ORC_OK)
+        st = orc_emit(0, par, tok, cur, (int32_t)emitted, max_path, accept_len, path, out_tokens);
+    status[0] = st;
+    if (st != ORC_OK) orc_accept_fail(0, max_path, accept_len, path, out_tokens);
+    return 0;
+}
+
 /* Rejection sampling along a chain draft ([P3] step 4; [P4] 无损性保障).
  * Node k (1..K, K = N-1) carries draft token x_k drawn from q row k; p row
  * k-1 is the target distribution for that position.  For k = 1..K:
@@ -373,7 +494,7 @@ static int64_t orc_sample_weights(const uint64_t* w, int64_t V, uint32_t x) {
  * subtraction) using word1 of the same draw; if those weights sum to 0 it is
  * sampled from weight(p_{k-1,t}) instead.  When all K drafts are accepted,
  * the bonus token is sampled from weight(p_{K,t}) with word1 of draw (b, K+1).
- * Trees that are not chains give ORC_UNSUPPORTED. */
+ * Trees that are not chains go to orc_accept_stochastic_tree. */
 int orc_accept_stochastic(const int32_t* parents, const int32_t* tokens, const float* p,
                           const float* q, int64_t B, int64_t N, int64_t V, uint64_t seed,
                           uint64_t offset, int64_t max_path, int32_t* accept_len, int32_t* path,
@@ -383,8 +504,16 @@ int orc_accept_stochastic(const int32_t* parents, const int32_t* tokens, const f
         const int32_t* par = parents + b * N;
         const int32_t* tok = tokens + b * N;
         int st = orc_check_tree(par, N);
-        for (int64_t i = 1; st == ORC_OK && i < N; ++i)
-            if (par[i] != i - 1) st = ORC_UNSUPPORTED;
+        int is_chain = 1;
+        for (int64_t i = 1; i < N; ++i)
+            if (par[i] != i - 1) is_chain = 0;
+        if (st == ORC_OK && !is_chain) {
+            orc_accept_stochastic_tree(parents + b * N, tokens + b * N, p + b * N * V,
+                                       q + b * N * V, 1, N, V, seed, offset, max_path,
+                                       accept_len + b, path + b * max_path,
+                                       out_tokens + b * max_path, status + b, b);
+            continue;
+        }
         for (int64_t c = 1; st == ORC_OK && c < N; ++c)
             if (tok[c] < 0 || tok[c] >= V) st = ORC_OUT_OF_RANGE;
         if (st == ORC_OK && max_path < 1) st = ORC_OUT_OF_RANGE;

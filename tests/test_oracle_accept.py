@@ -248,12 +248,147 @@ def test_disjoint_supports_always_reject_and_resample_from_target(orc):
     assert (freq[4:] == 0).all() and (out[:, 1:] == -1).all()
 
 
-def test_stochastic_rejects_non_chain_and_bad_tokens(orc):
+def test_stochastic_takes_branching_trees_and_rejects_bad_tokens(orc):
     p = np.full((3, 3, 4), 0.25, np.float32)
     par = np.array([[-1, 0, 0], [-1, 0, 1], [-1, 0, 1]], np.int32)
     tok = np.array([[0, 1, 2], [0, 4, 1], [0, 1, 2]], np.int32)
     acc, path, out, st = orc.accept_stochastic(par, tok, p, p, seed=0, offset=0, max_path=3)
-    assert list(st) == [orc.UNSUPPORTED, orc.OUT_OF_RANGE, 0]
+    assert list(st) == [0, orc.OUT_OF_RANGE, 0]
+    # p == q: the first child of the root is accepted, then node 1 is a leaf
+    assert acc[0] == 1 and list(path[0]) == [0, 1, -1] and out[0, 0] == 1
+
+
+# ---- branching trees: multi-candidate rejection sampling ------------------------
+
+TREE = np.array([-1, 0, 0, 0, 1, 1, 2], np.int32)  # root: 3 children; node 1: 2; node 2: 1
+
+
+def tree_inputs(rng, B, V, seed_rows):
+    """Target rows p[node] and draft rows q[node] = Q[parent(node)] (siblings are
+    drawn i.i.d. from their parent's draft distribution), tokens sampled from q."""
+    N = len(TREE)
+    pr = np.random.default_rng(seed_rows)
+    p = pr.dirichlet(np.ones(V) * 0.7, size=N).astype(np.float32)
+    Qp = pr.dirichlet(np.ones(V) * 0.7, size=N).astype(np.float32)
+    q = np.zeros((N, V), np.float32)
+    for c in range(1, N):
+        q[c] = Qp[TREE[c]]
+    tok = np.zeros((B, N), np.int32)
+    for c in range(1, N):
+        cdf = np.cumsum(q[c].astype(np.float64))
+        tok[:, c] = np.minimum(np.searchsorted(cdf / cdf[-1], rng.random(B)), V - 1)
+    return p, q, tok
+
+
+def test_tree_rejection_sampling_reproduces_target_distribution(orc):
+    """Whatever the tree's branching, the first emitted token follows the root's
+    target row, and given that node 1 was accepted the next one follows p[1]
+    (lossless speculative sampling, "vLLM EAGLE in practice", 无损性保障)."""
+    rng = np.random.default_rng(77)
+    V, B = 8, 250_000
+    p, q, _ = tree_inputs(rng, B, V, 3)
+    N = len(TREE)
+    par = np.tile(TREE, (B, 1))
+    P = np.broadcast_to(p, (B, N, V))
+    Qb = np.broadcast_to(q, (B, N, V))
+    first, second = [], []
+    for offset in range(4):
+        _, _, tok = tree_inputs(rng, B, V, 3)
+        acc, path, out, st = orc.accept_stochastic(par, tok, P, Qb, seed=5, offset=offset,
+                                                   max_path=4)
+        assert (st == 0).all()
+        first.append(out[:, 0])
+        via1 = (acc >= 1) & (path[:, 1] == 1)
+        second.append(out[via1, 1])
+    for sample, target in ((np.concatenate(first), p[0]), (np.concatenate(second), p[1])):
+        counts = np.bincount(sample, minlength=V)
+        expect = target.astype(np.float64) / target.sum() * len(sample)
+        keep = expect > 5
+        chi2 = ((counts[keep] - expect[keep]) ** 2 / expect[keep]).sum()
+        assert stats.chi2.sf(chi2, keep.sum() - 1) > 1e-4, (counts, expect)
+        tv = 0.5 * np.abs(counts / len(sample) - target / target.sum()).sum()
+        assert tv < 5e-3
+
+
+def test_tree_rule_reduces_to_the_chain_rule_on_chains(orc):
+    """The branching-tree routine run on chains gives exactly the chain routine's
+    accept lengths, paths and tokens (same draws, same integer CDF)."""
+    rng = np.random.default_rng(8)
+    B, N, V = 3000, 6, 64
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    par = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    a = orc.accept_stochastic(par, tok, p, q, seed=11, offset=3, max_path=N)
+    t = orc.accept_stochastic_tree(par, tok, p, q, seed=11, offset=3, max_path=N)
+    for x, y in zip(a, t):
+        assert np.array_equal(x, y)
+    assert 0 < (a[0] > 0).mean() < 1  # both outcomes occur
+
+
+def test_tree_identical_draft_and_target_takes_first_children(orc):
+    """q of every child equal to its parent's target row: the first child is
+    always accepted, so the path follows first children to a leaf."""
+    rng = np.random.default_rng(9)
+    V, B = 16, 2000
+    N = len(TREE)
+    p = rng.dirichlet(np.ones(V), size=(B, N)).astype(np.float32)
+    q = np.zeros_like(p)
+    for c in range(1, N):
+        q[:, c] = p[:, TREE[c]]
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    acc, path, out, st = orc.accept_stochastic(np.tile(TREE, (B, 1)), tok, p, q, seed=2,
+                                               offset=0, max_path=4)
+    # first children: 0 -> 1 -> 4 (a leaf); tokens with p = 0 never occur here
+    ok = p[np.arange(B), 0, tok[:, 1]] > 0
+    ok &= p[np.arange(B), 1, tok[:, 4]] > 0
+    assert (st == 0).all()
+    assert (acc[ok] == 2).all() and (path[ok, :3] == [0, 1, 4]).all()
+
+
+def test_tree_disjoint_supports_reject_every_child_and_resample_from_target(orc):
+    """Drafts only where the target is zero: every child of the root is tried and
+    rejected, and the emitted token follows the target row."""
+    V, B = 8, 20000
+    N = len(TREE)
+    p = np.zeros((B, N, V), np.float32)
+    q = np.zeros((B, N, V), np.float32)
+    p[:, :, :4] = [0.1, 0.2, 0.3, 0.4]
+    q[:, :, 4:] = 0.25
+    tok = np.tile(np.array([0, 5, 6, 7, 4, 5, 6], np.int32), (B, 1))
+    acc, path, out, st = orc.accept_stochastic(np.tile(TREE, (B, 1)), tok, p, q, seed=4,
+                                               offset=1, max_path=4)
+    assert (st == 0).all() and (acc == 0).all()
+    freq = np.bincount(out[:, 0], minlength=V) / B
+    np.testing.assert_allclose(freq[:4], [0.1, 0.2, 0.3, 0.4], atol=0.015)
+    assert (freq[4:] == 0).all()
+
+
+def test_tree_second_child_acceptance_matches_the_residual(orc):
+    """Root with two children, both drafted from q: after the first is rejected,
+    the second is accepted with probability sum_x q(x) min(1, r(x)/q(x)) =
+    sum_x min(q(x), r(x)), r = norm(max(0, p - q)) (the residual's overlap)."""
+    rng = np.random.default_rng(12)
+    V, B = 6, 400_000
+    par2 = np.array([-1, 0, 0], np.int32)
+    p0 = np.array([0.05, 0.3, 0.1, 0.25, 0.2, 0.1], np.float32)
+    qd = np.array([0.3, 0.1, 0.2, 0.1, 0.2, 0.1], np.float32)
+    p = np.broadcast_to(np.stack([p0, p0, p0]), (B, 3, V))
+    q = np.broadcast_to(np.stack([qd, qd, qd]), (B, 3, V))
+    cdf = np.cumsum(qd.astype(np.float64))
+    tok = np.zeros((B, 3), np.int32)
+    for c in (1, 2):
+        tok[:, c] = np.minimum(np.searchsorted(cdf, rng.random(B)), V - 1)
+    acc, path, out, st = orc.accept_stochastic(np.tile(par2, (B, 1)), tok, p, q, seed=6,
+                                               offset=0, max_path=2)
+    assert (st == 0).all()
+    r = np.maximum(0.0, p0.astype(np.float64) - qd)
+    r /= r.sum()
+    first_rej = ~((acc == 1) & (path[:, 1] == 1))
+    second_acc = (acc == 1) & (path[:, 1] == 2)
+    rate = second_acc.sum() / first_rej.sum()
+    assert abs(rate - np.minimum(qd, r).sum()) < 4e-3
+    assert abs((1 - first_rej.mean()) - np.minimum(p0, qd).sum()) < 3e-3
 
 
 def test_stochastic_draws_depend_on_seed_offset_and_sequence(orc):
