@@ -811,8 +811,150 @@ __device__ int chunk_find(const float* a, const float* bq, int lo, int hi, uint6
     return sfound;
 }
 
+// Stochastic acceptance on a branching tree, walked by one CTA for sequence b
+// (multi-candidate rejection sampling: the children of the current node are
+// tried in node order).  The first child of a node takes the chain's exact
+// test; after a rejection the target is the residual max(0, p - q) kept as
+// exact integer weights: after the first rejected child c,
+// w_t = weight(p_cur,t - q_c,t); after each further one c',
+// w_t <- max(0, w_t - floor(weight(q_c',t) * S / 2^40)) with S the sum before.
+// A later child c' is accepted iff u24 * weight(q_c'(x)) * S < w_x * 2^64.
+// All children rejected: the token is drawn from the residual (from the target
+// row when it has no mass) with word 1 of the last rejected child's draw; a
+// leaf: the bonus token from the target row with word 1 of draw N (leaf N-1) or
+// N + leaf.  The residual is recomputed element by element from the rows.
+__device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar, const int* stok) {
+    const int N = p.N, V = p.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ int rj[64];          // rejected children of the current node, in order
+    __shared__ uint64_t rS[64];     // residual sum after each of those rejections
+    __shared__ uint64_t tred[CH_WARPS];
+    __shared__ int tfound;
+    const float* tgt = p.target + (int64_t)b * N * V;
+    const float* drf = p.draft + (int64_t)b * N * V;
+    // weight of element t: target row (m == 0) or residual after m rejections
+    auto wt = [&](const float* pc, int m, int t) -> uint64_t {
+        if (m == 0) return weight(__ldg(pc + t));
+        uint64_t w = weight(__fsub_rn(__ldg(pc + t), __ldg(drf + (int64_t)rj[0] * V + t)));
+        for (int j = 1; j < m; ++j) {
+            const uint64_t qw = weight(__ldg(drf + (int64_t)rj[j] * V + t));
+            const uint64_t S = rS[j - 1];
+            const uint64_t d = (__umul64hi(qw, S) << 24) | ((qw * S) >> 40);  // floor(qw * S / 2^40)
+            w = w > d ? w - d : 0ull;
+        }
+        return w;
+    };
+    auto block_sum = [&](const float* pc, int m) -> uint64_t {
+        uint64_t sacc = 0;
+        for (int t = tid; t < V; t += CH_THREADS) sacc += wt(pc, m, t);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+        __syncthreads();
+        if (lane == 0) tred[warp] = sacc;
+        __syncthreads();
+        uint64_t tot = 0;
+#pragma unroll
+        for (int i = 0; i < CH_WARPS; ++i) tot += tred[i];
+        return tot;
+    };
+    // smallest t whose inclusive prefix sum exceeds T = floor(x * S / 2^32); -1 if S == 0
+    auto sample = [&](const float* pc, int m, uint64_t S, uint32_t x) -> int {
+        if (S == 0) return -1;
+        const uint64_t T = (uint64_t)x * (S >> 32) + (((uint64_t)x * (S & 0xffffffffull)) >> 32);
+        if (tid == 0) tfound = -1;
+        uint64_t run = 0;
+        for (int base = 0; base < V; base += CH_THREADS * 8) {
+            uint64_t e[8], sacc = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int t = base + tid * 8 + k;
+                e[k] = (t < V) ? wt(pc, m, t) : 0ull;
+                sacc += e[k];
+            }
+            uint64_t incl = sacc;  // inclusive scan over the warp's lanes
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            __syncthreads();
+            if (lane == 31) tred[warp] = incl;
+            __syncthreads();
+            uint64_t wpre = 0, total = 0;
+#pragma unroll
+            for (int i = 0; i < CH_WARPS; ++i) {
+                wpre += (i < warp) ? tred[i] : 0ull;
+                total += tred[i];
+            }
+            const uint64_t excl = run + wpre + (incl - sacc);
+            if (excl <= T && T < excl + sacc) {
+                uint64_t r = excl;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    r += e[k];
+                    if (r > T) {
+                        tfound = base + tid * 8 + k;
+                        break;
+                    }
+                }
+            }
+            if (run + total > T) break;
+            run += total;
+        }
+        __syncthreads();
+        return tfound;
+    };
+    int cur = 0, token = -1;
+    for (;;) {
+        const float* pc = tgt + (int64_t)cur * V;
+        int m = 0, next = -1, last_rej = -1;
+        uint64_t S = 0;
+        for (int c = cur + 1; c < N; ++c) {
+            if (spar[c] != cur) continue;
+            const uint32_t u24 = draw(p, b, c).x >> 8;
+            const int x = stok[c];
+            const float qx = __ldg(drf + (int64_t)c * V + x);
+            bool acc;
+            if (m == 0) {
+                acc = __dmul_rn((double)u24, (double)qx) < __dmul_rn((double)__ldg(pc + x), 16777216.0);
+            } else {
+                const uint64_t A = (uint64_t)u24 * weight(qx);  // < 2^64
+                acc = __umul64hi(A, S) < wt(pc, m, x);
+            }
+            if (acc) {
+                next = c;
+                break;
+            }
+            __syncthreads();  // earlier readers of rj / rS are done
+            if (tid == 0) rj[m] = c;
+            __syncthreads();
+            S = block_sum(pc, m + 1);
+            if (tid == 0) rS[m] = S;
+            __syncthreads();
+            ++m;
+            last_rej = c;
+            if (S == 0) break;
+        }
+        if (next >= 0) {
+            cur = next;
+            continue;
+        }
+        if (last_rej < 0) {  // a leaf: bonus token from the target row
+            const uint32_t x1 = draw(p, b, (cur == N - 1) ? N : N + cur).y;
+            token = sample(pc, 0, block_sum(pc, 0), x1);
+        } else {
+            const uint32_t x1 = draw(p, b, last_rej).y;
+            token = (S > 0) ? sample(pc, m, S, x1) : sample(pc, 0, block_sum(pc, 0), x1);
+        }
+        break;
+    }
+    if (token < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+    else write_path(p, b, spar, stok, cur, token);
+}
+
 // Stochastic chain acceptance: CTA (b, c) takes chunk c of the row the token
 // is drawn from; ws: sums[b][ceil(V / PIECE)] (weight sum of every piece), seq_tick[b].
+// A sequence whose tree is not a chain is walked by its chunk-0 CTA alone
+// (tree_walk_stochastic); its other CTAs return.
 template <bool VEC>
 __global__ void __launch_bounds__(CH_THREADS)
 accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
@@ -822,7 +964,7 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     const int b = blockIdx.x / ch, c = blockIdx.x % ch;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
     __shared__ int spar[64], stok[64];
-    __shared__ int sflag, skstar, last;
+    __shared__ int sflag, skstar, last, schain;
     __shared__ uint64_t red[STG][CH_WARPS];
     __shared__ uint64_t tsum[PIECE / 256];
     extern __shared__ __align__(1024) float ring_buf[];  // [STG][2][PIECE]
@@ -837,13 +979,23 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V, true);
-        if (tid == 0) sflag = f;
+        const int f = check_inputs(spar, stok, N, p.V, false);
+        bool branch = false;
+        for (int i = lane; i < N; i += 32) branch |= (i > 0 && spar[i] != i - 1);
+        branch = __any_sync(0xffffffffu, branch);
+        if (tid == 0) {
+            sflag = f;
+            schain = !branch;
+        }
     }
     __syncthreads();
     if (sflag != TV_OK) {
         if (c == 0) write_fail(p, b, sflag);
         return;  // every CTA of the sequence returns here: its counter is untouched
+    }
+    if (!schain) {
+        if (c == 0) tree_walk_stochastic(p, b, spar, stok);
+        return;  // the counter is untouched for a tree as well
     }
     // accept tests k = 1..K, all at once (counter-based draws); the first failure wins
     const int K = N - 1;

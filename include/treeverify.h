@@ -61,8 +61,7 @@ typedef enum {
     TV_ERR_INVALID_ARG = 1,  /* host: null pointer, bad size or shape            */
     TV_ERR_BAD_TREE = 2,     /* device: parent array violates the conventions     */
     TV_ERR_OUT_OF_RANGE = 3, /* device: block id, position, token id or length    */
-    TV_ERR_UNSUPPORTED = 4,  /* host: shape/dtype not built; device: stochastic
-                                acceptance on a tree that is not a chain          */
+    TV_ERR_UNSUPPORTED = 4,  /* host: shape/dtype not built                       */
     TV_ERR_CUDA = 5,         /* host: a CUDA runtime call or launch failed        */
     TV_ERR_TIMEOUT = 6,      /* device: a bounded wait ran out                    */
     TV_ERR_BAD_VALUES = 7,   /* device: an all-NaN logit row or a zero-mass
@@ -160,8 +159,9 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
  *   are those whose whole root path matches; the chosen node is the deepest
  *   accepted node (ties: smallest id).  The bonus token is the argmax of the
  *   chosen node's row.  draft_probs is ignored (may be NULL).
- * TV_ACCEPT_STOCHASTIC (chains only, parents[i] = i - 1): draft_probs
- *   [B][N][V] row k is the draft distribution node k's token was drawn from.
+ * TV_ACCEPT_STOCHASTIC: draft_probs [B][N][V] row k is the draft
+ *   distribution node k's token was drawn from.  On a chain (parents[i] =
+ *   i - 1):
  *   For k = 1..N-1, with (w0, w1, w2, w3) = Philox4x32-10(counter = (k, b,
  *   offset_lo, offset_hi), key = (seed_lo, seed_hi)) and u = w0 >> 8:
  *   accept x_k iff u * draft_probs[k][x_k] < target[k-1][x_k] * 2^24 (exact).
@@ -172,14 +172,28 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
  *   weights r uses integer weights floor(min(r,1) * 2^40) (0 for NaN or
  *   r <= 0), their exact sum S, T = floor(w1 * S / 2^32), and returns the
  *   smallest index whose inclusive prefix sum exceeds T.
+ *   On a branching tree (this rule is the library's: the pages fix only that
+ *   the result follows the target distribution) the children of the current
+ *   node cur are tried in node order.  The first is tested as above against
+ *   target[cur].  After a rejection the target is the residual, kept as the
+ *   integer weights w (sum S): after the first rejected child c, w_t =
+ *   weight(target[cur][t] - draft_probs[c][t]); after each further rejected
+ *   child c', w_t -= min(w_t, floor(weight(draft_probs[c'][t]) * S / 2^40))
+ *   with S before the update.  A later child c' (token x) is accepted iff
+ *   u * weight(draft_probs[c'][x]) * S < w_x * 2^64.  An accepted child
+ *   becomes cur.  When every child is rejected the token is drawn from w
+ *   (from target[cur] if S = 0, and then no later child is tried) with w1
+ *   of the last rejected child's draw; when cur is a leaf the bonus token is
+ *   drawn from target[cur] with w1 of the draw for k = N (leaf N-1) or
+ *   k = N + cur.  On a chain both descriptions agree.  A tree is walked by
+ *   one CTA per sequence.
  *
  * Outputs: accept_len int32 [B] = depth of the chosen node (number of
  * accepted drafts); path int32 [B][max_path] = node ids root..chosen, then
  * -1; out_tokens int32 [B][max_path] = the accepted drafts' tokens followed
  * by the bonus/correction token, then -1.  status int32 [B].  On a data
  * error (TV_ERR_BAD_TREE, TV_ERR_OUT_OF_RANGE for a token outside [0, V) or
- * a path longer than max_path, TV_ERR_UNSUPPORTED for a non-chain in
- * stochastic mode, TV_ERR_BAD_VALUES) the sequence gets accept_len 0, path
+ * a path longer than max_path, TV_ERR_BAD_VALUES) the sequence gets accept_len 0, path
  * [0, -1, ...] and out_tokens all -1.
  * workspace: at least tree_accept_workspace() bytes (0 means none is needed
  * and NULL is allowed).  Greedy acceptance on small batches reads every row

@@ -389,8 +389,60 @@ def test_stochastic_accept_paths_small(tv, orc, V):
     got = run_accept(tv, w, 1, N, seed=99, offset=5)
     ref = orc.accept_stochastic(par, tok, p, q, 99, 5, N)
     assert_same(got, ref)
-    assert ref[3][3] == orc.UNSUPPORTED and ref[3][4] == orc.OUT_OF_RANGE
+    assert ref[3][3] == orc.OK and ref[3][4] == orc.OUT_OF_RANGE  # a tree is walked
     assert (ref[0][~mix] == N - 1).sum() > 0
+
+
+def random_tree(rng, N, branch):
+    par = np.full(N, -1, np.int32)
+    kids = np.zeros(N, int)
+    for i in range(1, N):
+        cand = [j for j in range(i) if kids[j] < branch]
+        par[i] = rng.choice(cand)
+        kids[par[i]] += 1
+    return par
+
+
+@pytest.mark.parametrize("V", [8, 4099, 128256])
+def test_stochastic_accept_branching_trees(tv, orc, V):
+    """Multi-candidate rejection sampling on random trees: accept lengths, paths
+    and tokens bit-exact against the oracle, including drafts equal to the
+    target (deep acceptance), drafts disjoint from it (every child rejected),
+    a NaN target row and a zero-mass target row."""
+    rng = np.random.default_rng(V + 3)
+    B = 40 if V > 10000 else 300
+    N = 12
+    par = np.stack([random_tree(rng, N, 3) for _ in range(B)])
+    p = rng.dirichlet(np.ones(V) * 0.3, size=(B, N)).astype(np.float32)
+    qpar = rng.dirichlet(np.ones(V) * 0.3, size=(B, N)).astype(np.float32)
+    q = np.zeros_like(p)
+    for b in range(B):
+        for c in range(1, N):
+            q[b, c] = qpar[b, par[b, c]]
+    same = rng.random(B) < 0.3                          # drafts equal to the target
+    for b in np.nonzero(same)[0]:
+        for c in range(1, N):
+            q[b, c] = p[b, par[b, c]]
+    tok = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            cdf = np.cumsum(q[b, c].astype(np.float64))
+            tok[b, c] = min(int(np.searchsorted(cdf / cdf[-1], rng.random())), V - 1)
+    if V >= 8:
+        p[1, :, : V // 2] = 0.0                          # disjoint supports: reject every child
+        p[1] /= p[1].sum(axis=1, keepdims=True)
+        q[1, :, V // 2:] = 0.0
+        q[1] /= np.maximum(q[1].sum(axis=1, keepdims=True), 1e-30)
+        tok[1, 1:] = rng.integers(0, V // 2, size=N - 1)
+    p[2, 0, :] = np.nan
+    p[3, 0, :] = 0.0
+    w = {"parents": par, "draft_tokens": tok, "p": p, "q_probs": q}
+    max_path = N
+    got = run_accept(tv, w, 1, max_path, seed=21, offset=9)
+    ref = orc.accept_stochastic(par, tok, p, q, 21, 9, max_path)
+    assert_same(got, ref)
+    assert (ref[0][same & (np.arange(B) >= 4)] >= 1).all()
+    assert ref[0][3] == 0 and ref[3][3] == orc.BAD_VALUES
 
 
 # ------------------------------------------------------------------ compaction
