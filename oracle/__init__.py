@@ -170,6 +170,30 @@ def accept_stochastic_tree(parents, tokens, p, q, seed, offset, max_path):
     return acc, path, out, status
 
 
+def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_lens,
+                   rope_theta=0.0):
+    """In-place append of the tree's K/V rows into numpy caches -> status.
+
+    k_new / v_new [B][N][Hkv][d] and the caches [num_blocks][Hkv][bs][d] are
+    float32 arrays or bfloat16 bit patterns (uint16)."""
+    lib = _load()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    elem = 1 if k_cache.dtype == np.uint16 else 0
+    k_new = np.ascontiguousarray(k_new)
+    v_new = np.ascontiguousarray(v_new)
+    B, N, Hkv, d = k_new.shape
+    num_blocks, _, bs, _ = k_cache.shape
+    block_table = _c(block_table, np.int32)
+    prefix_lens = _c(prefix_lens, np.int32)
+    dep = _c(depth, np.int32) if depth is not None else np.zeros((B, N), np.int32)
+    status = np.zeros(B, np.int32)
+    lib.orc_tree_kv_append(I64(elem), _p(k_new), _p(v_new), _p(dep), I64(B), I64(N), I64(Hkv),
+                           I64(d), ctypes.c_double(rope_theta), _p(k_cache), _p(v_cache),
+                           _p(block_table), I64(block_table.shape[1]), _p(prefix_lens), I64(bs),
+                           I64(num_blocks), _p(status))
+    return status
+
+
 def philox4x32_10(counter, key):
     """One Philox4x32-10 block: counter 4 x uint32, key 2 x uint32 -> 4 x uint32."""
     lib = _load()

@@ -570,6 +570,83 @@ int orc_accept_stochastic(const int32_t* parents, const int32_t* tokens, const f
 }
 
 /* ------------------------------------------------------------------ */
+/* tree K/V append ([P2] KVCache.cat; the tree's rows go after the prefix) */
+/* ------------------------------------------------------------------ */
+
+/* Round a double to binary32 (nearest even), then to the cache element type
+ * (elem 1: bfloat16, nearest even on the binary32 bits; NaN kept quiet). */
+static void orc_store(int elem, void* base, int64_t idx, double x) {
+    float f = (float)x;
+    if (elem == 0) {
+        ((float*)base)[idx] = f;
+        return;
+    }
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t h;
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) {
+        h = (uint16_t)((u >> 16) | 0x0040u);
+    } else {
+        u += 0x7FFFu + ((u >> 16) & 1u);
+        h = (uint16_t)(u >> 16);
+    }
+    ((uint16_t*)base)[idx] = h;
+}
+
+/* Node i of sequence b goes to logical position t = P_b + i of both caches
+ * ([num_blocks][Hkv][bs][d]), every kv head.  With rope_theta > 0 the key is
+ * first rotated by position P_b + depth[b][i] (rotate-half pairs (j, j + d/2),
+ * j < d/2, angle pos * rope_theta^(-2j/d), in double):
+ *   k'_j = k_j cos - k_{j+d/2} sin,   k'_{j+d/2} = k_{j+d/2} cos + k_j sin;
+ * values (and keys when rope_theta <= 0) are copied unchanged.  A sequence
+ * with P_b < 0, a depth outside [0, N) (rope only) or a position without a
+ * valid block gets ORC_OUT_OF_RANGE and no write. */
+int orc_tree_kv_append(int64_t elem, const void* k_new, const void* v_new, const int32_t* depth,
+                       int64_t B, int64_t N, int64_t Hkv, int64_t d, double rope_theta,
+                       void* k_cache, void* v_cache, const int32_t* block_table,
+                       int64_t max_blocks, const int32_t* prefix_lens, int64_t bs,
+                       int64_t num_blocks, int32_t* status) {
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t P = prefix_lens[b];
+        int st = ORC_OK;
+        if (P < 0) st = ORC_OUT_OF_RANGE;
+        for (int64_t i = 0; st == ORC_OK && i < N; ++i) {
+            if (orc_slot(block_table, max_blocks, b, P + i, bs, num_blocks) < 0) st = ORC_OUT_OF_RANGE;
+            if (rope_theta > 0.0 && (depth[b * N + i] < 0 || depth[b * N + i] >= N))
+                st = ORC_OUT_OF_RANGE;
+        }
+        status[b] = st;
+        if (st != ORC_OK) continue;
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t slot = orc_slot(block_table, max_blocks, b, P + i, bs, num_blocks);
+            const int64_t blk = slot / bs, row = slot % bs;
+            for (int64_t g = 0; g < Hkv; ++g) {
+                const int64_t src = ((b * N + i) * Hkv + g) * d;
+                const int64_t dst = ((blk * Hkv + g) * bs + row) * d;
+                for (int64_t e = 0; e < d; ++e)
+                    orc_store((int)elem, v_cache, dst + e, orc_load((int)elem, v_new, src + e));
+                if (rope_theta <= 0.0) {
+                    for (int64_t e = 0; e < d; ++e)
+                        orc_store((int)elem, k_cache, dst + e, orc_load((int)elem, k_new, src + e));
+                    continue;
+                }
+                const double pos = (double)(P + depth[b * N + i]);
+                const int64_t h = d / 2;
+                for (int64_t j = 0; j < h; ++j) {
+                    const double ang = pos * pow(rope_theta, -2.0 * (double)j / (double)d);
+                    const double c = cos(ang), sn = sin(ang);
+                    const double x1 = orc_load((int)elem, k_new, src + j);
+                    const double x2 = orc_load((int)elem, k_new, src + j + h);
+                    orc_store((int)elem, k_cache, dst + j, x1 * c - x2 * sn);
+                    orc_store((int)elem, k_cache, dst + j + h, x2 * c + x1 * sn);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* KV compaction ([P2] KVCache.copy: index_select -> narrow -> copy_)   */
 /* ------------------------------------------------------------------ */
 
