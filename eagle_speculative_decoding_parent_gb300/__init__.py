@@ -23,7 +23,7 @@ from . import _build
 __all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTED",
            "TV_ERR_TIMEOUT", "TV_ERR_BAD_VALUES", "TV_F32", "TV_BF16", "GREEDY", "STOCHASTIC",
            "TreeVerifyError", "library_path", "status_string", "tree_mask_build",
-           "tree_verify_attention_workspace", "tree_verify_attention_kernels",
+           "tree_verify_attention_workspace", "tree_verify_attention_kernels", "tree_kv_append",
            "tree_verify_attention",
            "tree_verify_attention_noalloc", "tree_verify_attention_noalloc_capacity",
            "tree_accept_workspace",
@@ -65,6 +65,8 @@ _abi = _sig("tv_abi_version", _i, [])
 _mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p])
 _attn_ws = _sig("tree_verify_attention_workspace", _sz, [_i, _i, _i, _i, _i, _i, _i, _i])
 _attn_nk = _sig("tree_verify_attention_kernels", _i, [_i, _i, _i, _i, _i, _i, _i, _i, _sz])
+_append = _sig("tree_kv_append", _i, [_p, _p, _p, _i, _i, _i, _i, _f, _p, _p, _p, _i, _p, _i, _i,
+                                      _i, _p, _p])
 _attn = _sig("tree_verify_attention", _i,
              [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p])
 _attn_na = _sig("tree_verify_attention_noalloc", _i,
@@ -194,6 +196,18 @@ def tree_accept(mode, parents, draft_tokens, target, draft_probs, accept_len, pa
     _check(_acc(mode, _ptr(parents), _ptr(draft_tokens), _ptr(target), _ptr(draft_probs), B, N,
                 V, seed, offset, _ptr(accept_len), _ptr(path), _ptr(out_tokens), path.shape[1],
                 _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)), "tree_accept")
+
+
+def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_lens, status, *,
+                   rope_theta: float = 0.0, stream=None) -> None:
+    """k_new / v_new [B,N,Hkv,d]; caches [num_blocks,Hkv,bs,d]; depth int32 [B,N]
+    (needed when rope_theta > 0); status int32 [B]."""
+    B, N, Hkv, d = k_new.shape
+    num_blocks, _, bs, _ = k_cache.shape
+    _check(_append(_ptr(k_new), _ptr(v_new), _ptr(depth), B, N, Hkv, d, float(rope_theta),
+                   _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                   _ptr(prefix_lens), bs, num_blocks, _dt(k_cache), _ptr(status), _stream(stream)),
+           "tree_kv_append")
 
 
 def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, new_lens, status,

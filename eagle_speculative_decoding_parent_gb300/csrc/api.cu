@@ -171,6 +171,29 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
     return launch_accept(a);
 }
 
+tv_status tree_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B, int N,
+                         int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* prefix_lens, int block_size, int num_blocks, tv_dtype dt,
+                         int32_t* status, tv_stream_t stream) {
+    if (dt != TV_F32 && dt != TV_BF16) return TV_ERR_INVALID_ARG;
+    const int eb = dt == TV_F32 ? 4 : 2;
+    if (B < 0 || N < 1 || N > 64 || Hkv < 1 || d < 2 || (d & 1) || block_size < 1 ||
+        num_blocks < 1 || max_blocks_per_seq < 1 || !(rope_theta == rope_theta))
+        return TV_ERR_INVALID_ARG;
+    if ((d * eb) % 16 != 0) return TV_ERR_UNSUPPORTED;
+    if (B == 0) return TV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_table || !prefix_lens || !status ||
+        (rope_theta > 0.f && !depth))
+        return TV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15) ||
+        (reinterpret_cast<uintptr_t>(k_cache) & 15) || (reinterpret_cast<uintptr_t>(v_cache) & 15))
+        return TV_ERR_INVALID_ARG;
+    return launch_kv_append(k_new, v_new, depth, B, N, Hkv, d, rope_theta, k_cache, v_cache,
+                            block_table, max_blocks_per_seq, prefix_lens, block_size, num_blocks,
+                            eb, status, (cudaStream_t)stream);
+}
+
 tv_status kv_compact(void* k_cache, void* v_cache, int num_layers, int64_t layer_stride,
                      const int32_t* block_table, int max_blocks_per_seq,
                      const int32_t* prefix_lens, const int32_t* path, const int32_t* accept_len,

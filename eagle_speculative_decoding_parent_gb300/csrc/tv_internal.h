@@ -95,6 +95,10 @@ tv_status launch_attn_tc(const AttnArgs& a);
 // bytes of it that must be zero when a call starts
 size_t attn_tc_workspace(int B, int N, int Hq, int Hkv);
 size_t attn_tc_zeroed_prefix(int B, int N, int Hq, int Hkv);
+tv_status launch_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B,
+                           int N, int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                           const int32_t* block_table, int max_blocks, const int32_t* prefix_lens,
+                           int bs, int num_blocks, int elem, int32_t* status, cudaStream_t stream);
 // kernels one tensor-core attention call launches with this workspace size
 int attn_tc_kernels(int B, int N, int Hq, int Hkv, size_t ws_bytes);
 // Leading bytes of that workspace that must be zero when a call starts.

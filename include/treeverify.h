@@ -215,6 +215,35 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
                       size_t workspace_bytes, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_kv_append — "EAGLE code principles", KV缓存优化: KVCache.cat appends
+ * the new tokens' K/V after the prefix.  The step before
+ * tree_verify_attention ("write then attend"): node i of sequence b sits at
+ * logical position t = P_b + i (physical slot block_table[b][t / block_size]
+ * * block_size + t % block_size).
+ *
+ * k_new, v_new: [B][N][Hkv][d] (dt elements), the tree's keys and values.
+ * For every node and kv head the value row, and the key row when
+ * rope_theta <= 0, is copied to the node's slot of v_cache / k_cache
+ * ([num_blocks][Hkv][block_size][d]).  With rope_theta > 0 the key is first
+ * rotated by its tree position P_b + depth[b][i] (depth int32 [B][N], e.g.
+ * from tree_mask_build): rotate-half pairs (j, j + d/2), j < d/2, angle
+ * pos * rope_theta^(-2j/d):
+ *   k'_j = k_j cos - k_{j+d/2} sin,  k'_{j+d/2} = k_{j+d/2} cos + k_j sin,
+ * every product and sum in double, rounded to float32, then to dt.
+ * status int32 [B]: TV_ERR_OUT_OF_RANGE for P_b < 0, a position
+ * P_b .. P_b+N-1 without a valid block, or (rotation only) a depth outside
+ * [0, N); such a sequence's cache is left unchanged.
+ * Host errors: N outside [1, 64], d odd, d * element size not a multiple of
+ * 16 bytes (TV_ERR_UNSUPPORTED), a NULL depth with rope_theta > 0, NaN
+ * rope_theta, pointers not 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+tv_status tree_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B, int N,
+                         int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                         const int32_t* block_table, int max_blocks_per_seq,
+                         const int32_t* prefix_lens, int block_size, int num_blocks, tv_dtype dt,
+                         int32_t* status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * kv_compact — "EAGLE code principles", KV缓存优化: KVCache.copy(indices,
  * prev_length) selects the kept rows (index_select), locates the
  * destination (narrow at prev_length) and copies them there; "P-EAGLE in

@@ -445,6 +445,61 @@ def test_stochastic_accept_branching_trees(tv, orc, V):
     assert ref[0][3] == 0 and ref[3][3] == orc.BAD_VALUES
 
 
+# ------------------------------------------------------------------ K/V append
+
+@pytest.mark.parametrize("bf16,theta", [(True, 500000.0), (True, 0.0), (False, 10000.0)])
+def test_kv_append_matches_oracle(tv, orc, bf16, theta):
+    """Tree K/V rows into the paged cache at P + i, keys rotated by P + depth(i):
+    copies bit-exact; rotated keys equal to the oracle's up to one unit in the
+    last place of the cache type (double-precision sin/cos/pow of the device and
+    of the host library may differ in their last bit); a bad block, a negative
+    prefix and a bad depth leave their sequences untouched with status 3."""
+    rng = np.random.default_rng(int(theta) % 97 + bf16)
+    B, N, Hkv, d, bs = 6, 26, 8, 128, 16
+    P = rng.integers(0, 3000, size=B).astype(np.int32)
+    nb = [(int(x) + N + bs - 1) // bs for x in P]
+    maxb = max(nb)
+    perm = rng.permutation(sum(nb) + 4)
+    table = np.full((B, maxb), -1, np.int32)
+    k = 0
+    for b in range(B):
+        table[b, :nb[b]] = perm[k:k + nb[b]]
+        k += nb[b]
+    num_blocks = sum(nb) + 4
+    mk = (lambda a: W.f32_to_bf16_bits(a.astype(np.float32))) if bf16 else (lambda a: a.astype(np.float32))
+    kc = mk(rng.standard_normal((num_blocks, Hkv, bs, d)))
+    vc = mk(rng.standard_normal((num_blocks, Hkv, bs, d)))
+    kn = mk(rng.standard_normal((B, N, Hkv, d)) * 3)
+    vn = mk(rng.standard_normal((B, N, Hkv, d)))
+    depth = np.stack([orc.tree_mask(random_tree(rng, N, 3)[None])[1][0] for _ in range(B)]).astype(np.int32)
+    table[1, int(P[1]) // bs] = num_blocks + 2           # bad block
+    P[2] = -5                                            # negative prefix
+    if theta > 0:
+        depth[3, 7] = N                                  # bad depth (rotation only)
+    kr, vr = kc.copy(), vc.copy()
+    st_ref = orc.tree_kv_append(kn, vn, depth, kr, vr, table, P, rope_theta=theta)
+    to = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()) if bf16 else \
+        (lambda a: torch.from_numpy(a).cuda())
+    kd, vd = to(kc), to(vc)
+    st = torch.full((B,), -9, dtype=torch.int32, device="cuda")
+    tv.tree_kv_append(to(kn), to(vn), dev(depth), kd, vd, dev(table), dev(P), st, rope_theta=theta)
+    torch.cuda.synchronize()
+    back = (lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)) if bf16 else \
+        (lambda t: t.cpu().numpy())
+    kg, vg = back(kd), back(vd)
+    assert list(st.cpu().numpy()) == list(st_ref)
+    assert st_ref[1] == orc.OUT_OF_RANGE and st_ref[2] == orc.OUT_OF_RANGE
+    assert np.array_equal(vg, vr)
+    if theta <= 0:
+        assert np.array_equal(kg, kr)
+        return
+    bits = np.uint16 if bf16 else np.uint32
+    diff = np.abs(kg.view(bits).astype(np.int64) - kr.view(bits).astype(np.int64))
+    assert diff.max() <= 1, diff.max()
+    assert (diff > 0).mean() < 1e-3
+    assert not np.array_equal(kg, kc)                    # keys were written
+
+
 # ------------------------------------------------------------------ compaction
 
 def run_compact(tv, k, v, bt, P, path, acc, bf16, num_layers=1, layer_stride=0):
