@@ -2,7 +2,8 @@
 
 A convenience for callers that hold torch tensors: it owns the outputs and
 the attention workspace and issues, in stream order,
-tree_mask_build -> tree_verify_attention -> tree_accept -> kv_compact.
+tree_mask_build -> tree_verify_attention -> tree_accept -> kv_compact,
+eagerly (``run``) or as a captured CUDA graph (``capture``, then replay).
 Marshalling only; the arithmetic is in the CUDA library.
 """
 from __future__ import annotations
@@ -62,6 +63,26 @@ class VerifyStep:
         self.attention(q, k_cache, v_cache, block_table, prefix_lens, stream)
         self.accept(mode, parents, draft_tokens, target, draft_probs, seed, offset, stream)
         self.compact(k_cache, v_cache, block_table, prefix_lens, stream)
+
+    def capture(self, **step_args) -> "torch.cuda.CUDAGraph":
+        """Records one step (the four launches of ``run`` with these tensors) into
+        a CUDA graph; ``graph.replay()`` then re-issues it with one launch.  The
+        graph keeps the tensors' addresses and the host-side choices of this call
+        (schedule, tensor descriptors): refill the same input tensors in place
+        between replays and keep the shapes.  One eager step first takes the
+        library's one-time host set-up (function attributes, occupancy queries),
+        so none of it is recorded; the caches are mutated by that step like by
+        any other (compaction)."""
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            self.run(**step_args, stream=stream)
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run(**step_args, stream=torch.cuda.current_stream())
+        return graph
 
 
 __all__ = ["VerifyStep", "GREEDY", "STOCHASTIC"]

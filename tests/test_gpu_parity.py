@@ -559,6 +559,54 @@ def test_compaction_bit_exact(tv, orc, bf16, num_layers):
 
 # ------------------------------------------------------------------ whole step
 
+@pytest.mark.parametrize("name", ["llama3_8b_tree60", "llama3_8b_b128_chain5"])
+def test_graph_replay_matches_eager_step(tv, name):
+    """The step captured as a CUDA graph and replayed gives the same outputs and
+    cache contents, bit for bit, as the eager step on the same inputs."""
+    from eagle_speculative_decoding_parent_gb300.pipeline import VerifyStep
+    spec = W.SPECS[name]
+    w = W.make(name)
+    B, N = w["parents"].shape
+    mp = W.max_path_len(w["parents"])
+    mode = 0 if spec.mode == "greedy" else 1
+
+    def fresh():
+        return to_device(w)
+
+    def make_step(d):
+        return VerifyStep(B=B, N=N, Hq=spec.Hq, Hkv=spec.Hkv, d=spec.d,
+                          max_blocks=w["block_table"].shape[1], bs=spec.bs, dtype=d["q"].dtype,
+                          max_path=mp, V=spec.V, mode=mode)
+
+    def args(d):
+        return dict(parents=d["parents"], q=d["q"], k_cache=d["k_cache"], v_cache=d["v_cache"],
+                    block_table=d["block_table"], prefix_lens=d["prefix_lens"],
+                    draft_tokens=d["draft_tokens"], target=d["logits"] if mode == 0 else d["p"],
+                    draft_probs=None if mode == 0 else d["q_probs"], mode=mode,
+                    seed=w.get("seed", 0), offset=w.get("offset", 0))
+
+    def outputs(st, d):
+        torch.cuda.synchronize()
+        return [t.cpu().clone() for t in (st.out, st.accept_len, st.path, st.out_tokens,
+                                          st.new_lens, d["k_cache"], d["v_cache"])]
+
+    d1 = fresh()
+    s1 = make_step(d1)
+    s1.run(**args(d1))
+    ref = outputs(s1, d1)
+    d2 = fresh()
+    s2 = make_step(d2)
+    graph = s2.capture(**args(d2))      # one eager step, then the recording
+    orig = fresh()
+    d2["k_cache"].copy_(orig["k_cache"])  # undo that step's compaction, same addresses
+    d2["v_cache"].copy_(orig["v_cache"])
+    graph.replay()
+    got = outputs(s2, d2)
+    for a, b in zip(ref, got):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.uint8) if b.dtype == torch.bfloat16 else b)
+
+
 @pytest.mark.parametrize("name", list(W.SPECS))
 def test_full_step_matches_oracle(tv, orc, name):
     """mask -> attention -> accept -> compaction on the GPU, each output
