@@ -166,20 +166,17 @@ __device__ void write_path(const AccParams& p, int b, const int* spar, const int
 
 // Tree and token checks in the order the acceptance rule states them
 // (structure first, then token range).  One full warp; result in every lane.
-__device__ int check_inputs(const int* spar, const int* stok, int N, int V, bool chain) {
+__device__ int check_inputs(const int* spar, const int* stok, int N, int V) {
     const int lane = threadIdx.x & 31;
-    bool tree_bad = false, chain_bad = false, tok_bad = false;
+    bool tree_bad = false, tok_bad = false;
     for (int i = lane; i < N; i += 32) {
         const int pa = spar[i];
         tree_bad |= (i == 0 && pa != -1) || (i > 0 && (pa < 0 || pa >= i));
-        chain_bad |= (i > 0 && pa != i - 1);
         tok_bad |= (i > 0 && (stok[i] < 0 || stok[i] >= V));
     }
     const bool any_tree = __any_sync(0xffffffffu, tree_bad);
-    const bool any_chain = __any_sync(0xffffffffu, chain_bad);
     const bool any_tok = __any_sync(0xffffffffu, tok_bad);
     if (any_tree) return TV_ERR_BAD_TREE;
-    if (chain && any_chain) return TV_ERR_UNSUPPORTED;
     if (any_tok) return TV_ERR_OUT_OF_RANGE;
     return TV_OK;
 }
@@ -460,7 +457,7 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     }
     __syncthreads();
     if (tid < 32) {
-        int f = check_inputs(spar, stok, N, p.V, false);
+        int f = check_inputs(spar, stok, N, p.V);
         bool late = false;
         for (int k = tid; k < N; k += 32) late |= (sam[k] == TIMED_OUT);
         const bool any_late = __any_sync(0xffffffffu, late);
@@ -506,7 +503,7 @@ accept_walk_kernel(AccParams p) {
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V, false);
+        const int f = check_inputs(spar, stok, N, p.V);
         if (tid == 0) sflag = f;
     }
     __syncthreads();
@@ -979,7 +976,7 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V, false);
+        const int f = check_inputs(spar, stok, N, p.V);
         bool branch = false;
         for (int i = lane; i < N; i += 32) branch |= (i > 0 && spar[i] != i - 1);
         branch = __any_sync(0xffffffffu, branch);

@@ -502,7 +502,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     };
 
     if (warp == 0 || warp == 2) {
-        // ==== producers: warp 0 loads Q and pages 0-1 of each tile, warp 2 pages 2-3 ====
+        // ==== producers: warp 0 loads pages 0-1 of each tile, warp 2 pages 2-3 ====
         // (two warps on different schedulers: each issues half of a tile's copies;
         // a page is two K boxes, one per 64-column half, and one V box)
         const bool kprod = (warp == 0);
