@@ -78,6 +78,19 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert k(1, 4, 6, 4, 128, 10, 16, 1, 0) == -1     # Hq not a multiple of Hkv
     assert k(1, 65, 8, 2, 128, 10, 16, 1, 0) == -1    # more than 64 nodes
     assert k(0, 4, 8, 2, 128, 10, 16, 1, 0) == 0
+    # tree_kv_append: host-side argument checks (nothing is launched)
+    ap = lib.tree_kv_append
+    ap.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                   p, p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
+    args = lambda B, N, Hkv, d, theta, depth, dt=1: (nz, nz, depth, B, N, Hkv, d, theta, nz, nz,
+                                                     nz, 4, nz, 16, 10, dt, nz, None)
+    assert ap(*args(1, 65, 2, 128, 0.0, nz)) == 1          # more than 64 nodes
+    assert ap(*args(1, 4, 2, 127, 0.0, nz)) == 1           # odd head size
+    assert ap(*args(1, 4, 2, 4, 0.0, nz)) == 4             # 8-byte rows: not 16-byte vectors
+    assert ap(*args(1, 4, 2, 128, 10000.0, None)) == 1     # rotation without depth
+    assert ap(*args(1, 4, 2, 128, float("nan"), nz)) == 1  # NaN theta
+    assert ap(*args(0, 4, 2, 128, 0.0, nz)) == 0           # empty batch: nothing to do
+    assert ap(*args(1, 4, 2, 128, 0.0, nz, dt=7)) == 1     # unknown dtype
     # kv_compact: rows that are not a multiple of 16 bytes -> unsupported
     c = lib.kv_compact
     c.argtypes = [p, p, ctypes.c_int, ctypes.c_int64, p, ctypes.c_int, p, p, p] + \
