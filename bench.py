@@ -55,6 +55,23 @@ def dist_env():
     return rank, world, local
 
 
+def slowest_rank(ms: float, world: int, device="cuda") -> float:
+    """The largest of every rank's `ms` (an all-reduce MAX); `ms` itself alone."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, B: int, N: int, ms_per_step: float) -> float:
+    """Tokens per second of the whole job: every rank verifies its own B x N nodes
+    per step, and the job's step time is the slowest rank's."""
+    return world * B * N / (ms_per_step * 1e-3)
+
+
 # ---------------------------------------------------------------- algorithmic work
 
 def attn_bytes(w) -> int:
@@ -342,12 +359,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     per = np.array([[kev[k][j].elapsed_time(kev[k][j + 1]) for j in range(4)]
                     for k in range(args.steps)])  # ms: mask, attn, accept, compact
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank(total_ms, world)
     ms_per_step = total_ms / args.steps
-    value = world * B * N / (ms_per_step * 1e-3)
+    value = whole_job_rate(world, B, N, ms_per_step)
     acc_len = step.accept_len.cpu().numpy()
     names = ["tree_mask_build", "tree_verify_attention", "tree_accept", "kv_compact"]
     mean_ms = per.mean(axis=0)
@@ -413,11 +427,7 @@ def run_ours(args):
         b.record(stream)
         b.synchronize()
         e_ms.append(a.elapsed_time(b))
-    e2e_ms = float(np.mean(e_ms))
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank(float(np.mean(e_ms)), world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -431,7 +441,7 @@ def run_ours(args):
                 "config": workload_config(w),
                 "roofline": roofline,
                 "cpu_baseline": cpu,
-                "e2e": {"value": world * B * N / (e2e_ms * 1e-3), "unit": UNIT,
+                "e2e": {"value": whole_job_rate(world, B, N, e2e_ms), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": (3 + attn_kernels) * args.steps,
                 "clocks": clocks,
