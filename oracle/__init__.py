@@ -19,6 +19,12 @@ Parity status of each function (the pins are in ``tests/test_oracle_*.py``):
                     integer-CDF check)
   kv_compact        pinned (torch index_select + narrow + copy_, the operation
                     the KVCache.copy passage describes)
+  tree_kv_append    pinned (closed-form rotations, plain copies, error cases)
+  draft_tree        pinned (exhaustive enumeration of every token path when no
+                    pruning can bite, greedy-chain and one-layer closed forms,
+                    per-layer frontier / final cut recomputed with numpy and
+                    scipy on a path-keyed draft model, hand-worked fixture,
+                    tie and breadth-first-label cases)
 """
 from __future__ import annotations
 
@@ -238,3 +244,102 @@ def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, *,
                        I64(Hkv), I64(d), I64(bs), I64(num_blocks), _p(new_lens), _p(src),
                        _p(dst), _p(status))
     return new_lens, src, dst, status
+
+
+class DraftTree:
+    """Draft-tree construction for one sequence, one layer per ``expand`` call
+    (the draft model runs between layers on the frontier the call returns).
+
+    Node 0 is the root (``root_token``, score 0).  ``expand(rows)`` takes the
+    draft logits float32 [F, V] of the current frontier (F = 1 at the first
+    layer, the root) and returns (front_tokens, front_src): the next frontier
+    best first, and for each entry the row it was drawn from.  ``finalize(N)``
+    returns (parents int32 [N], tokens int32 [N], scores float64 [N], status).
+    ``margin`` is the smallest score gap behind any ranking decision so far.
+    """
+
+    def __init__(self, root_token: int, V: int, k: int, layers: int):
+        self.V, self.k, self.layers = V, k, layers
+        cap = 1 + k + max(0, layers - 1) * k * k
+        self.tok = np.zeros(cap, np.int32)
+        self.par = np.full(cap, -1, np.int32)
+        self.score = np.zeros(cap, np.float64)
+        self.tok[0] = root_token
+        self.count = 1
+        self.front = np.zeros(1, np.int32)
+        self.margin = np.inf
+        self.status = OK
+
+    def front_paths(self):
+        """Token path (root token excluded) of every frontier node."""
+        out = []
+        for u in self.front:
+            p = []
+            while u > 0:
+                p.append(int(self.tok[u]))
+                u = self.par[u]
+            out.append(tuple(reversed(p)))
+        return out
+
+    def expand(self, rows):
+        lib = _load()
+        rows = _c(rows, np.float32)
+        F = len(self.front)
+        assert rows.shape == (F, self.V)
+        nf = min(self.k, F * self.k)
+        new_front = np.zeros(nf, np.int32)
+        new_src = np.zeros(nf, np.int32)
+        m = ctypes.c_double(self.margin)
+        st = lib.orc_draft_expand(I64(self.V), I64(self.k), I64(F), _p(rows), _p(self.front),
+                                  _p(self.tok), _p(self.par), _p(self.score),
+                                  I64(self.count), _p(new_front), _p(new_src), ctypes.byref(m))
+        if st != OK:
+            self.status = st
+            return None, None
+        self.margin = m.value
+        self.count += F * self.k
+        self.front = new_front
+        return self.tok[new_front].copy(), new_src
+
+    def finalize(self, N: int):
+        lib = _load()
+        parents = np.full(N, -1, np.int32)
+        tokens = np.full(N, -1, np.int32)
+        scores = np.full(N, -np.inf, np.float64)
+        if self.status != OK:
+            return parents, tokens, scores, self.status
+        m = ctypes.c_double(self.margin)
+        st = lib.orc_draft_finalize(I64(self.count), _p(self.tok), _p(self.par), _p(self.score),
+                                    I64(N), _p(parents), _p(tokens), _p(scores), ctypes.byref(m))
+        self.margin = m.value
+        return parents, tokens, scores, st
+
+
+def draft_tree(rows_per_layer, root_tokens, k: int, N: int):
+    """Batch driver: rows_per_layer[l] float32 [B, F_l, V] (F_0 = 1, then k),
+    rows in the order of the previous layer's frontier.  Returns (parents
+    [B, N], tokens [B, N], scores [B, N] float64, fronts, status [B], margin [B])
+    with fronts[l] = (front_tokens [B, k], front_src [B, k]), -1 where a
+    sequence failed."""
+    B = len(root_tokens)
+    L = len(rows_per_layer)
+    V = rows_per_layer[0].shape[-1]
+    trees = [DraftTree(int(root_tokens[b]), V, k, L) for b in range(B)]
+    fronts = []
+    for rows in rows_per_layer:
+        ft = np.full((B, k), -1, np.int32)
+        fs = np.full((B, k), -1, np.int32)
+        for b, t in enumerate(trees):
+            if t.status != OK:
+                continue
+            a, s = t.expand(rows[b])
+            if a is not None:
+                ft[b, :len(a)], fs[b, :len(s)] = a, s
+        fronts.append((ft, fs))
+    out = [t.finalize(N) for t in trees]
+    parents = np.stack([o[0] for o in out])
+    tokens = np.stack([o[1] for o in out])
+    scores = np.stack([o[2] for o in out])
+    status = np.array([o[3] for o in out], np.int32)
+    margin = np.array([t.margin for t in trees])
+    return parents, tokens, scores, fronts, status, margin

@@ -38,7 +38,11 @@
  *     exactly; residual max(0, p - q) sampled through an integer CDF with
  *     2^-40 resolution; on a branching tree the children of a node are tried
  *     in node order with the residual carried in exact integer weights; see
- *     orc_accept_stochastic and orc_accept_stochastic_tree.
+ *     orc_accept_stochastic and orc_accept_stochastic_tree;
+ *   - draft-tree construction: top-k children per expanded node by draft
+ *     logit, cumulative log-probability scores, the k best new nodes expanded
+ *     next, the N - 1 best nodes kept and labelled breadth-first; see
+ *     orc_draft_expand and orc_draft_finalize.
  *
  * Parity pins live in tests/test_oracle_*.py.
  */
@@ -718,4 +722,154 @@ int orc_kv_compact(int64_t elem_bytes, void* k_cache, void* v_cache, int64_t num
 /* Exposes the integer-CDF sampler to the tests (pinned exhaustively there). */
 int64_t orc_sample_weights_u32(const uint64_t* w, int64_t V, uint32_t x) {
     return orc_sample_weights(w, V, x);
+}
+
+/* ------------------------------------------------------------------ */
+/* draft-tree construction ([P1] EnhancedEagleProposer: multi-level    */
+/* candidate generation and path pruning; [P2] tree buffers: keep the  */
+/* high-probability paths, prune the low-probability branches)         */
+/* ------------------------------------------------------------------ */
+
+/* Readings (the pages give the outline only):
+ *   - a node's draft row is log-softmax'ed; its candidate children are the k
+ *     tokens with the largest logits (ties: lowest token id);
+ *   - a node's score is its path's cumulative draft log-probability,
+ *     score(child) = score(parent) + logit - logsumexp(row);
+ *   - nodes are numbered in creation order: frontier node f's children are
+ *     created f-major, child rank j minor;
+ *   - the next frontier is the k best nodes created in this layer, by
+ *     (score descending, creation id ascending), in that rank order;
+ *   - the final tree keeps the root and the N - 1 best other nodes by the
+ *     same order, relabelled breadth-first from the root with every node's
+ *     children visited in creation order.
+ * `margin` (in/out) takes the minimum over every ranking decision of the
+ * score gap that decided it, so a caller can tell when another precision
+ * could rank differently. */
+
+/* The k largest entries of row[0..V) by (value desc, index asc). */
+static void orc_row_topk(const float* row, int64_t V, int64_t k, int64_t* idx) {
+    int64_t n = 0;
+    for (int64_t t = 0; t < V; ++t) {
+        if (n == k && !((double)row[t] > (double)row[idx[k - 1]])) continue;
+        int64_t pos = (n < k) ? n++ : k - 1;
+        while (pos > 0 && (double)row[t] > (double)row[idx[pos - 1]]) {
+            idx[pos] = idx[pos - 1];
+            --pos;
+        }
+        idx[pos] = t;
+    }
+}
+
+static const double* orc_sort_score;
+static int orc_by_score(const void* a, const void* b) {
+    const int32_t u = *(const int32_t*)a, v = *(const int32_t*)b;
+    if (orc_sort_score[u] > orc_sort_score[v]) return -1;
+    if (orc_sort_score[u] < orc_sort_score[v]) return 1;
+    return (u > v) - (u < v);
+}
+
+/* One layer: rows[F][V] are the draft logits after frontier nodes
+ * front[0..F) (creation ids).  Appends F*k nodes at ids count.. and writes
+ * the next frontier (min(k, F*k) ids, best first) and, per frontier entry,
+ * the row it came from.  Returns ORC_OK, or ORC_BAD_VALUES for a NaN or +inf
+ * logit or a row without a finite logit (nothing is appended then). */
+int orc_draft_expand(int64_t V, int64_t k, int64_t F, const float* rows, const int32_t* front,
+                     int32_t* tok, int32_t* par, double* score, int64_t count,
+                     int32_t* new_front, int32_t* new_src, double* margin) {
+    double* lse = (double*)malloc(sizeof(double) * F);
+    for (int64_t f = 0; f < F; ++f) {
+        const float* row = rows + f * V;
+        double m = -INFINITY;
+        for (int64_t t = 0; t < V; ++t) {
+            if (isnan(row[t]) || row[t] == INFINITY) { free(lse); return ORC_BAD_VALUES; }
+            if ((double)row[t] > m) m = row[t];
+        }
+        if (m == -INFINITY) { free(lse); return ORC_BAD_VALUES; }
+        double s = 0.0;
+        for (int64_t t = 0; t < V; ++t) s += exp((double)row[t] - m);
+        lse[f] = m + log(s);
+    }
+    int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * k);
+    for (int64_t f = 0; f < F; ++f) {
+        orc_row_topk(rows + f * V, V, k, idx);
+        for (int64_t j = 0; j < k; ++j) {
+            const int64_t id = count + f * k + j;
+            tok[id] = (int32_t)idx[j];
+            par[id] = front[f];
+            score[id] = score[front[f]] + ((double)rows[f * V + idx[j]] - lse[f]);
+        }
+    }
+    const int64_t M = F * k;
+    int32_t* ord = (int32_t*)malloc(sizeof(int32_t) * M);
+    for (int64_t i = 0; i < M; ++i) ord[i] = (int32_t)(count + i);
+    orc_sort_score = score;
+    qsort(ord, (size_t)M, sizeof(int32_t), orc_by_score);
+    const int64_t nf = M < k ? M : k;
+    for (int64_t r = 0; r < nf; ++r) {
+        new_front[r] = ord[r];
+        new_src[r] = (int32_t)((ord[r] - count) / k);
+    }
+    /* the frontier's order decides later creation ids, its boundary decides membership */
+    for (int64_t r = 0; r + 1 < M && r < nf; ++r) {
+        const double gap = score[ord[r]] - score[ord[r + 1]];
+        if (gap < *margin) *margin = gap;
+    }
+    free(ord);
+    free(idx);
+    free(lse);
+    return ORC_OK;
+}
+
+/* Final tree from the C created nodes (node 0 = root): the root plus the N - 1
+ * best others, breadth-first.  parents/tokens [N], scores [N].  Returns
+ * ORC_OK, or ORC_BAD_TREE when a kept node's parent was not kept. */
+int orc_draft_finalize(int64_t C, const int32_t* tok, const int32_t* par, const double* score,
+                       int64_t N, int32_t* parents, int32_t* tokens, double* scores,
+                       double* margin) {
+    int32_t* ord = (int32_t*)malloc(sizeof(int32_t) * (C > 1 ? C - 1 : 1));
+    for (int64_t i = 1; i < C; ++i) ord[i - 1] = (int32_t)i;
+    orc_sort_score = score;
+    qsort(ord, (size_t)(C - 1), sizeof(int32_t), orc_by_score);
+    if (N - 1 < C - 1 && N > 1) {
+        const double gap = score[ord[N - 2]] - score[ord[N - 1]];
+        if (gap < *margin) *margin = gap;
+    }
+    char* kept = (char*)calloc((size_t)C, 1);
+    kept[0] = 1;
+    for (int64_t r = 0; r < N - 1; ++r) kept[ord[r]] = 1;
+    /* breadth-first from the root: a queue, children in creation order */
+    int32_t* queue = (int32_t*)malloc(sizeof(int32_t) * N);
+    int32_t* label = (int32_t*)malloc(sizeof(int32_t) * C);
+    for (int64_t i = 0; i < C; ++i) label[i] = -1;
+    int64_t head = 0, tail = 0;
+    queue[tail++] = 0;
+    label[0] = 0;
+    while (head < tail) {
+        const int32_t u = queue[head++];
+        for (int64_t v = 1; v < C; ++v) {
+            if (kept[v] && par[v] == u && tail < N) {
+                label[v] = (int32_t)tail;
+                queue[tail++] = (int32_t)v;
+            }
+        }
+    }
+    int st = (tail == N) ? ORC_OK : ORC_BAD_TREE;
+    for (int64_t i = 0; i < N; ++i) {
+        parents[i] = -1;
+        tokens[i] = -1;
+        scores[i] = -INFINITY;
+    }
+    if (st == ORC_OK) {
+        for (int64_t i = 0; i < N; ++i) {
+            const int32_t u = queue[i];
+            parents[i] = (u == 0) ? -1 : label[par[u]];
+            tokens[i] = tok[u];
+            scores[i] = score[u];
+        }
+    }
+    free(label);
+    free(queue);
+    free(kept);
+    free(ord);
+    return st;
 }
