@@ -27,7 +27,7 @@ __all__ = ["TV_OK", "TV_ERR_BAD_TREE", "TV_ERR_OUT_OF_RANGE", "TV_ERR_UNSUPPORTE
            "tree_verify_attention",
            "tree_verify_attention_noalloc", "tree_verify_attention_noalloc_capacity",
            "tree_accept_workspace",
-           "tree_accept", "kv_compact"]
+           "tree_accept", "kv_compact", "draft_tree_workspace", "draft_tree_expand"]
 
 (TV_OK, TV_ERR_INVALID_ARG, TV_ERR_BAD_TREE, TV_ERR_OUT_OF_RANGE, TV_ERR_UNSUPPORTED,
  TV_ERR_CUDA, TV_ERR_TIMEOUT, TV_ERR_BAD_VALUES, TV_ERR_WORKSPACE) = range(9)
@@ -78,6 +78,10 @@ _acc = _sig("tree_accept", _i,
 _compact = _sig("kv_compact", _i,
                 [_p, _p, _i, _i64, _p, _i, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                  _p, _p])
+
+_dt_ws = _sig("draft_tree_workspace", _sz, [_i, _i, _i])
+_dt = _sig("draft_tree_expand", _i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p,
+                                      _sz, _p])
 
 assert _abi() == 1, "header / library ABI mismatch"
 
@@ -222,3 +226,31 @@ def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, new
                     max_path, B, Hkv, d, bs, num_blocks, _dt(k_cache), _ptr(new_lens),
                     _ptr(src_slots), _ptr(dst_slots), _ptr(status), _stream(stream)),
            "kv_compact")
+
+
+def draft_tree_workspace(B, topk, layers) -> int:
+    return int(_dt_ws(B, topk, layers))
+
+
+def draft_tree_expand(logits, layer, layers, status, workspace, *, topk, root_tokens=None,
+                      N=1, front_tokens=None, front_src=None, parents=None, tokens=None,
+                      scores=None, stream=None) -> None:
+    """One draft-tree layer: logits float32 [B, F, V] (F = 1 at layer 0, else
+    topk); root_tokens int32 [B] (layer 0); front_tokens / front_src int32
+    [B, topk]; on the last layer parents / tokens int32 [B, N] and scores
+    float32 [B, N]; workspace uint8 (zero-filled before the first call)."""
+    B, F, V = logits.shape
+    _want(logits, torch.float32, "logits")
+    _want(status, torch.int32, "status")
+    for t, n in ((root_tokens, "root_tokens"), (front_tokens, "front_tokens"),
+                 (front_src, "front_src"), (parents, "parents"), (tokens, "tokens")):
+        if t is not None:
+            _want(t, torch.int32, n)
+    if scores is not None:
+        _want(scores, torch.float32, "scores")
+    if F != (1 if layer == 0 else topk):
+        raise ValueError(f"layer {layer} takes {1 if layer == 0 else topk} rows per sequence")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_dt(_ptr(logits), _ptr(root_tokens), B, V, topk, layer, layers, N, _ptr(front_tokens),
+               _ptr(front_src), _ptr(parents), _ptr(tokens), _ptr(scores), _ptr(status),
+               _ptr(workspace), ws_bytes, _stream(stream)), "draft_tree_expand")

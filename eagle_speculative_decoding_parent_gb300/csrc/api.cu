@@ -240,4 +240,51 @@ tv_status kv_compact(void* k_cache, void* v_cache, int num_layers, int64_t layer
     return launch_compact(a);
 }
 
+size_t draft_tree_workspace(int B, int topk, int layers) {
+    if (B < 1 || topk < 1 || topk > DT_K_MAX || layers < 1) return 0;
+    if (draft_tree_nodes(topk, layers) > DT_NODES_MAX) return 0;
+    return draft_tree_ws_bytes(B, topk, layers);
+}
+
+tv_status draft_tree_expand(const float* logits, const int32_t* root_tokens, int B, int V, int topk,
+                            int layer, int layers, int N, int32_t* front_tokens,
+                            int32_t* front_src, int32_t* parents, int32_t* tokens, float* scores,
+                            int32_t* status, void* workspace, size_t workspace_bytes,
+                            tv_stream_t stream) {
+    if (B < 0 || V < 1 || V > (1 << 30) || topk < 1 || topk > DT_K_MAX || topk > V || layers < 1 ||
+        layer < 0 || layer >= layers || N < 1 || N > 64)
+        return TV_ERR_INVALID_ARG;
+    const int64_t nodes = draft_tree_nodes(topk, layers);
+    if (nodes > DT_NODES_MAX) return TV_ERR_UNSUPPORTED;
+    if (N > nodes) return TV_ERR_INVALID_ARG;
+    if (B == 0) return TV_OK;
+    const bool last = (layer == layers - 1);
+    if (!logits || !status || (layer == 0 && !root_tokens) || (last && (!parents || !tokens)))
+        return TV_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15) ||
+        workspace_bytes < draft_tree_ws_bytes(B, topk, layers))
+        return TV_ERR_WORKSPACE;
+    // grid: B x F rows x at most DT_CH_MAX chunks
+    if ((int64_t)B * topk * DT_CH_MAX > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+    DraftArgs a;
+    a.logits = logits;
+    a.root_tokens = root_tokens;
+    a.B = B;
+    a.V = V;
+    a.k = topk;
+    a.layer = layer;
+    a.layers = layers;
+    a.N = N;
+    a.front_tokens = front_tokens;
+    a.front_src = front_src;
+    a.parents = parents;
+    a.tokens = tokens;
+    a.scores = scores;
+    a.status = status;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    a.stream = (cudaStream_t)stream;
+    return launch_draft_expand(a);
+}
+
 }  // extern "C"

@@ -145,4 +145,30 @@ struct CompactArgs {
 };
 tv_status launch_compact(const CompactArgs& a);
 
+// Draft-tree construction limits: chunks per vocabulary row, top-k, nodes
+// created per tree (1 + k + (layers - 1) k^2).
+constexpr int DT_CH_MAX = 64;
+constexpr int DT_K_MAX = 16;
+constexpr int DT_NODES_MAX = 2048;
+
+struct DraftArgs {
+    const float* logits;
+    const int32_t* root_tokens;
+    int B, V, k, layer, layers, N;
+    int32_t* front_tokens;
+    int32_t* front_src;
+    int32_t* parents;
+    int32_t* tokens;
+    float* scores;
+    int32_t* status;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+int64_t draft_tree_nodes(int k, int layers);
+size_t draft_tree_ws_bytes(int B, int k, int layers);
+// chunks per row and chunk length of one layer's launch
+void draft_tree_chunks(int rows, int V, bool vec, int* c, int* per);
+tv_status launch_draft_expand(const DraftArgs& a);
+
 }  // namespace tv

@@ -66,7 +66,9 @@ typedef enum {
     TV_ERR_TIMEOUT = 6,      /* device: a bounded wait ran out                    */
     TV_ERR_BAD_VALUES = 7,   /* device: an all-NaN logit row or a zero-mass
                                 distribution where a token must be chosen         */
-    TV_ERR_WORKSPACE = 8     /* host: workspace missing or too small              */
+    TV_ERR_WORKSPACE = 8     /* host: workspace missing or too small; device
+                                (draft_tree_expand): no state from the previous
+                                layer in the workspace                          */
 } tv_status;
 
 typedef enum { TV_F32 = 0, TV_BF16 = 1 } tv_dtype;
@@ -269,6 +271,56 @@ tv_status kv_compact(void* k_cache, void* v_cache, int num_layers, int64_t layer
                      int max_path, int B, int Hkv, int d, int block_size, int num_blocks,
                      tv_dtype dt, int32_t* new_lens, int64_t* src_slots, int64_t* dst_slots,
                      int32_t* status, tv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * draft_tree_expand — "vLLM-TreeEagle", 核心组件 / 3. EnhancedEagleProposer
+ * (candidates generated over several levels, paths pruned) and "EAGLE code
+ * principles", 树结构缓冲 (likely paths precomputed, high-probability paths
+ * kept, low-probability branches cut).  The step before verification: the
+ * draft tree is grown one layer per call from the draft model's logits (the
+ * draft model runs between calls, on the frontier each call returns).
+ *
+ * logits: fp32 [B][F][V]; F = 1 at layer 0 (the row after the root, whose
+ * token is root_tokens[b]), F = topk at later layers (row f follows frontier
+ * entry f of the previous call).  Each row's topk largest logits (ties: lowest
+ * token id) become children, scored score(parent) + logit - logsumexp(row) in
+ * fp32 (the root scores 0).  Nodes are numbered in creation order: row-major,
+ * then rank.  The next frontier is the topk best new nodes by (score
+ * descending, creation id ascending): front_tokens int32 [B][topk] (their
+ * tokens, best first) and front_src int32 [B][topk] (the row each came from);
+ * both nullable.  The call for the last layer (layer == layers - 1) also
+ * writes the tree: the root and the N - 1 best of all created nodes, same
+ * order, labelled breadth-first from the root with each node's children in
+ * creation order (so 0 <= parents[i] < i, the order tree_mask_build and
+ * tree_accept expect): parents int32 [B][N] (-1 at the root), tokens int32
+ * [B][N] (tokens[b][0] = root token), scores fp32 [B][N] (nullable).
+ * status int32 [B], written by every call: TV_ERR_OUT_OF_RANGE for a root
+ * token outside [0, V) (layer 0), TV_ERR_BAD_VALUES for a NaN or +inf logit
+ * or a row without a finite one, TV_ERR_WORKSPACE when the workspace does not
+ * hold the sequence's state after layer - 1.  An error sticks for the later
+ * layers of the tree; the sequence's frontier outputs become -1, its tree
+ * parents and tokens -1 and its scores -inf.
+ * workspace: draft_tree_workspace() bytes, 16-byte aligned.  It holds
+ * per-sequence arrival counters that must be zero before the first call (zero
+ * the whole buffer once; every completed call leaves them at zero), the tree
+ * state carried from layer to layer, and per-chunk partial results.  The
+ * calls of one tree go in order layer 0, 1, ..., layers - 1 on one workspace;
+ * calls sharing a workspace must not run concurrently.
+ * Host errors: TV_ERR_INVALID_ARG for topk outside [1, 16] or above V, V
+ * outside [1, 2^30], layers < 1, layer outside [0, layers), N outside [1, 64]
+ * or above the number of created nodes 1 + topk + (layers - 1) * topk^2, a
+ * NULL logits or status, a NULL root_tokens at layer 0, a NULL parents or
+ * tokens at the last layer; TV_ERR_UNSUPPORTED for more than 2048 created
+ * nodes; TV_ERR_WORKSPACE for a missing, misaligned or small workspace.
+ * draft_tree_workspace returns 0 for unsupported sizes.
+ * ------------------------------------------------------------------------ */
+size_t draft_tree_workspace(int B, int topk, int layers);
+
+tv_status draft_tree_expand(const float* logits, const int32_t* root_tokens, int B, int V,
+                            int topk, int layer, int layers, int N, int32_t* front_tokens,
+                            int32_t* front_src, int32_t* parents, int32_t* tokens, float* scores,
+                            int32_t* status, void* workspace, size_t workspace_bytes,
+                            tv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * tree_verify_attention_noalloc — no counterpart on the pages describing the

@@ -97,3 +97,37 @@ def test_host_argument_checks_need_no_gpu(lib):
         [ctypes.c_int] * 7 + [p, p, p, p, p]
     assert c(nz, nz, 1, 0, nz, 4, nz, nz, nz, 4, 2, 2, 12, 16, 10, 1, nz, None, None, nz,
              None) == 4
+
+
+def test_draft_tree_host_checks(lib):
+    p, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    ws = lib.draft_tree_workspace
+    ws.restype, ws.argtypes = sz, [ci, ci, ci]
+    f = lib.draft_tree_expand
+    f.restype = ci
+    f.argtypes = [p, p, ci, ci, ci, ci, ci, ci, p, p, p, p, p, p, p, sz, p]
+    assert ws(2, 4, 3) > 0 and ws(2, 17, 3) == 0 and ws(0, 4, 3) == 0
+    assert ws(1, 16, 8) > 0 and ws(1, 16, 9) == 0           # 1809 / 2065 created nodes
+    need = ws(2, 4, 3)
+    buf = ctypes.create_string_buffer(need + 32)
+    a16 = (ctypes.addressof(buf) + 15) // 16 * 16
+    dev = p(0x1000)                                          # never dereferenced on the host
+
+    def call(B=2, V=100, k=4, layer=0, layers=3, N=10, logits=dev, root=dev, parents=dev,
+             tokens=dev, status=dev, wsp=p(a16), wsb=need):
+        return f(logits, root, B, V, k, layer, layers, N, None, None, parents, tokens, None,
+                 status, wsp, wsb, None)
+
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 4, 8
+    assert call(k=0) == INVALID and call(k=17) == INVALID and call(k=101) == INVALID
+    assert call(V=0) == INVALID and call(V=(1 << 30) + 1) == INVALID
+    assert call(layers=0) == INVALID and call(layer=3) == INVALID and call(layer=-1) == INVALID
+    assert call(N=0) == INVALID and call(N=65) == INVALID
+    assert call(k=1, layers=2, N=4) == INVALID               # only 3 nodes are ever created
+    assert call(k=16, layers=10, N=8) == UNSUPPORTED
+    assert call(B=-1) == INVALID and call(B=0) == 0
+    assert call(logits=None) == INVALID and call(status=None) == INVALID
+    assert call(root=None) == INVALID                        # layer 0 reads the root tokens
+    assert call(layer=2, parents=None) == INVALID and call(layer=2, tokens=None) == INVALID
+    assert call(wsp=None) == WORKSPACE and call(wsp=p(a16 + 4)) == WORKSPACE
+    assert call(wsb=need - 1) == WORKSPACE
