@@ -734,7 +734,10 @@ int64_t orc_sample_weights_u32(const uint64_t* w, int64_t V, uint32_t x) {
  *   - a node's draft row is log-softmax'ed; its candidate children are the k
  *     tokens with the largest logits (ties: lowest token id);
  *   - a node's score is its path's cumulative draft log-probability,
- *     score(child) = score(parent) + logit - logsumexp(row);
+ *     score(child) = score(parent) + (logit - logsumexp(row)), the logsumexp
+ *     in double rounded to binary32 and both operations in binary32: the
+ *     pages fix no precision, so the ranking decisions are taken in the
+ *     library's (binary32);
  *   - nodes are numbered in creation order: frontier node f's children are
  *     created f-major, child rank j minor;
  *   - the next frontier is the k best nodes created in this layer, by
@@ -796,7 +799,9 @@ int orc_draft_expand(int64_t V, int64_t k, int64_t F, const float* rows, const i
             const int64_t id = count + f * k + j;
             tok[id] = (int32_t)idx[j];
             par[id] = front[f];
-            score[id] = score[front[f]] + ((double)rows[f * V + idx[j]] - lse[f]);
+            /* ranked in binary32: logsumexp rounded once, then two binary32 operations */
+            const float logp = rows[f * V + idx[j]] - (float)lse[f];
+            score[id] = (double)((float)score[front[f]] + logp);
         }
     }
     const int64_t M = F * k;

@@ -8,6 +8,9 @@ high-probability ones, prune the rest); the oracle fills it in EAGLE-2 style
 N - 1 best nodes kept, breadth-first labels).  These tests check it against
 things fixed independently of its code:
 
+Scores are ranked in binary32 (the library's precision; the pages fix none),
+so they are compared with the double-precision recomputations within 5e-5.
+
 * exhaustive enumeration: when k >= N - 1 no pruning step can drop a node of
   the best N - 1 root paths (each of them has fewer than k better nodes at its
   own depth and among its siblings), so the tree must be exactly the N - 1
@@ -72,7 +75,7 @@ def test_equals_best_paths_of_exhaustive_enumeration(orc, seed, V, k, L, N):
     got = node_paths(par, tok)
     assert got[0] == () and set(got[1:]) == set(best)
     for p, s in zip(got[1:], sc[1:]):
-        assert abs(s - scores[p]) < 1e-9
+        assert abs(s - scores[p]) < 5e-5
 
 
 def test_chain_when_k_is_one(orc):
@@ -86,7 +89,7 @@ def test_chain_when_k_is_one(orc):
         t = int(np.argmax(row))
         s += float(log_softmax(row.astype(np.float64))[t])
         path.append(t)
-        assert tok[i] == t and abs(sc[i] - s) < 1e-9
+        assert tok[i] == t and abs(sc[i] - s) < 5e-5
     assert tok[0] == 11
 
 
@@ -101,7 +104,7 @@ def test_one_layer_is_the_root_rows_stable_argsort(orc):
     order = np.argsort(-row, kind="stable")
     assert list(tok[1:]) == list(order[:N - 1]) and list(tok[1:4]) == [3, 17, 25]
     assert (par[1:] == 0).all()
-    assert np.allclose(sc[1:], log_softmax(row.astype(np.float64))[order[:N - 1]], atol=1e-12)
+    assert np.allclose(sc[1:], log_softmax(row.astype(np.float64))[order[:N - 1]], atol=1e-6)
 
 
 @pytest.mark.parametrize("seed,V,k,L,N", [(11, 9, 2, 4, 8), (12, 7, 3, 4, 12), (13, 12, 4, 3, 20),
@@ -131,7 +134,7 @@ def test_pruned_construction_properties(orc, seed, V, k, L, N):
     best = sorted(created, key=lambda q: -created[q])[:N - 1]
     assert set(got[1:]) == set(best)
     for p, s in zip(got[1:], sc[1:]):
-        assert abs(s - created[p]) < 1e-9
+        assert abs(s - created[p]) < 5e-5
     # breadth-first labels: parents never decrease, siblings keep creation
     # (= draft-probability) order, depth never decreases
     assert all(par[i] <= par[i + 1] for i in range(1, N - 1))
