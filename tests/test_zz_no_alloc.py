@@ -8,8 +8,9 @@ workspace-taking entry point within the attention tolerance used everywhere
 else (bf16: max-abs 2e-2, mean-abs 2e-3), on two calls in a row, since every
 call reuses the same array and must clear what has to start at zero.
 
-This file is collected last so that a run stopping at its first failure has
-already run every other test; it also passes on its own in a fresh process.
+This file is collected after the parity tests so that a run stopping at its
+first failure has already run them; it also passes on its own in a fresh
+process.
 """
 import numpy as np
 import pytest

@@ -13,6 +13,9 @@ checks that the tree is a valid breadth-first draft tree whose sorted scores
 match the oracle's.  Rows are indexed by frontier position, so such a swap
 changes parent scores by less than the gap and leaves the score multiset
 within tolerance.
+
+This file is collected after every other test file: it covers the newest
+kernel, so a run stopping at its first failure has already run the rest.
 """
 import numpy as np
 import pytest
