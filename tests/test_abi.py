@@ -131,3 +131,19 @@ def test_draft_tree_host_checks(lib):
     assert call(layer=2, parents=None) == INVALID and call(layer=2, tokens=None) == INVALID
     assert call(wsp=None) == WORKSPACE and call(wsp=p(a16 + 4)) == WORKSPACE
     assert call(wsb=need - 1) == WORKSPACE
+
+
+def test_draft_tree_binding_checks_need_no_gpu(lib):
+    """The Python binding rejects wrong dtypes, a row count that does not match
+    the layer, and host tensors, before the library is called."""
+    torch = pytest.importorskip("torch")
+    import eagle_speculative_decoding_parent_gb300 as tv
+    st = torch.zeros(2, dtype=torch.int32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        tv.draft_tree_expand(torch.zeros(2, 1, 8, dtype=torch.float64), 0, 2, st, ws, topk=2)
+    with pytest.raises(ValueError, match="rows per sequence"):
+        tv.draft_tree_expand(torch.zeros(2, 1, 8), 1, 2, st, ws, topk=2)
+    with pytest.raises(ValueError, match="CUDA device"):
+        tv.draft_tree_expand(torch.zeros(2, 1, 8), 0, 2, st, ws, topk=2,
+                             root_tokens=torch.zeros(2, dtype=torch.int32))
