@@ -103,14 +103,29 @@ __device__ __forceinline__ void dt_warp_combine(float& m, float& s) {
     }
 }
 
+// One thread's running state over its logits, visited in increasing token order.
+// Once the list is full, a logit can enter only if its value is above the value
+// of the list's last word (an equal value has a higher token id than every
+// entry, so its word is smaller): one float comparison per logit, and the
+// 64-bit word is formed only for the few that enter.  The sum of exp uses the
+// hardware exponential (arguments <= 0; a few units in the last place for the
+// terms near the maximum, which carry the sum).
 template <int KP>
 struct DtTake {
     float m = -INFINITY, s = 0.f;
+    float thr = -INFINITY;  // value of top[KP - 1] once the list is full
+    bool full = false;
     bool bad = false;
     uint64_t top[KP];
     __device__ __forceinline__ DtTake() {
 #pragma unroll
         for (int i = 0; i < KP; ++i) top[i] = 0;
+    }
+    __device__ __forceinline__ void offer(float a, int t) {
+        if (full && !(a > thr)) return;
+        dt_offer<KP>(top, dt_word(a, t));
+        full = top[KP - 1] != 0;
+        if (full) thr = dt_unkey((uint32_t)(top[KP - 1] >> 32));
     }
     // four consecutive logits starting at token t
     __device__ __forceinline__ void take4(float a0, float a1, float a2, float a3, int t) {
@@ -120,11 +135,12 @@ struct DtTake {
             s = (m == -INFINITY) ? 0.f : s * expf(m - mx);
             m = mx;
         }
-        if (m > -INFINITY) s += (expf(a0 - m) + expf(a1 - m)) + (expf(a2 - m) + expf(a3 - m));
-        dt_offer<KP>(top, dt_word(a0, t));
-        dt_offer<KP>(top, dt_word(a1, t + 1));
-        dt_offer<KP>(top, dt_word(a2, t + 2));
-        dt_offer<KP>(top, dt_word(a3, t + 3));
+        if (m > -INFINITY)
+            s += (__expf(a0 - m) + __expf(a1 - m)) + (__expf(a2 - m) + __expf(a3 - m));
+        offer(a0, t);
+        offer(a1, t + 1);
+        offer(a2, t + 2);
+        offer(a3, t + 3);
     }
     __device__ __forceinline__ void take1(float a, int t) {
         bad |= !(a < INFINITY);
@@ -132,8 +148,8 @@ struct DtTake {
             s = (m == -INFINITY) ? 0.f : s * expf(m - a);
             m = a;
         }
-        if (m > -INFINITY) s += expf(a - m);
-        dt_offer<KP>(top, dt_word(a, t));
+        if (m > -INFINITY) s += __expf(a - m);
+        offer(a, t);
     }
 };
 
