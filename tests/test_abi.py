@@ -147,3 +147,16 @@ def test_draft_tree_binding_checks_need_no_gpu(lib):
     with pytest.raises(ValueError, match="CUDA device"):
         tv.draft_tree_expand(torch.zeros(2, 1, 8), 0, 2, st, ws, topk=2,
                              root_tokens=torch.zeros(2, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
+    """include/treeverify.h compiles on its own as C99 and as C++11, with no
+    CUDA header: the boundary carries only plain pointers and sizes."""
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    import subprocess
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-x", lang, HEADER], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
