@@ -1,4 +1,10 @@
-// draft_tree_expand: one layer of draft-tree construction per launch.
+// draft_tree_expand: one layer of draft-tree construction per launch
+// ("vLLM-TreeEagle", 核心组件 / 3. EnhancedEagleProposer: candidates generated
+// over several levels, paths pruned; "EAGLE code principles", 树结构缓冲:
+// high-probability paths kept, low-probability branches cut).  Filled in
+// EAGLE-2 style: top-k children per expanded node by draft logit, scores are
+// cumulative log-probabilities in binary32, the k best new nodes are expanded
+// next, and the last layer keeps the N - 1 best nodes.
 //
 // The draft rows of a layer ([B][F][V] fp32 logits, F = 1 at the first layer,
 // then k) are cut into chunks of the vocabulary, one CTA per (row, chunk).
