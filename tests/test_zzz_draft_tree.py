@@ -200,3 +200,24 @@ def test_draft_tree_workspace_reuse_and_order_check(tv, orc):
     tv.draft_tree_expand(rows, 1, L, status, fresh, topk=k)
     torch.cuda.synchronize()
     assert (status.cpu().numpy() == 8).all()             # no layer-0 state: TV_ERR_WORKSPACE
+
+
+def test_draft_tree_feeds_the_verification_step(tv, orc):
+    """The tree this call writes is what tree_mask_build takes: topological,
+    root first.  Its mask and depths equal the oracle's for the same parents."""
+    B, V, k, L, N = 4, 2048, 4, 5, 48
+    rows = draft_rows(61, B, V, k, L)
+    roots = np.array([1, 2, 3, 4])
+    gp, gt, gs, gf, gst = run_gpu(tv, rows, roots, k, N)
+    assert (gst == 0).all()
+    par = torch.from_numpy(gp).cuda()
+    mask = torch.zeros((B, N), dtype=torch.int64, device="cuda")
+    depth = torch.zeros((B, N), dtype=torch.int32, device="cuda")
+    status = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    tv.tree_mask_build(par, mask, depth, status)
+    torch.cuda.synchronize()
+    om, od, ost = orc.tree_mask(gp)
+    assert (status.cpu().numpy() == 0).all() and (ost == 0).all()
+    assert (mask.cpu().numpy().view(np.uint64) == om).all()
+    assert (depth.cpu().numpy() == od).all()
+    assert od.max() <= L
