@@ -79,9 +79,9 @@ _compact = _sig("kv_compact", _i,
                 [_p, _p, _i, _i64, _p, _i, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                  _p, _p])
 
-_dt_ws = _sig("draft_tree_workspace", _sz, [_i, _i, _i])
-_dt = _sig("draft_tree_expand", _i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p,
-                                      _sz, _p])
+_draft_ws = _sig("draft_tree_workspace", _sz, [_i, _i, _i])
+_draft_expand = _sig("draft_tree_expand", _i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p,
+                                               _p, _p, _p, _sz, _p])
 
 assert _abi() == 1, "header / library ABI mismatch"
 
@@ -107,9 +107,15 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _want(t, dtype, name):
+def _want(t, dtype, name, shape=None):
+    """Checks a tensor's dtype (and shape) before its pointer reaches the
+    library: the kernels index every buffer by the sizes passed beside it."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _stream(stream):
@@ -117,7 +123,7 @@ def _stream(stream):
     return s.cuda_stream
 
 
-def _dt(t):
+def _dtype_code(t):
     if t.dtype == torch.bfloat16:
         return TV_BF16
     if t.dtype == torch.float32:
@@ -128,8 +134,13 @@ def _dt(t):
 def tree_mask_build(parents, mask, depth, status, stream=None) -> None:
     """parents int32 [B,N] -> mask int64 (uint64 bits) [B,N], depth int32 [B,N] or None, status [B]."""
     _want(parents, torch.int32, "parents")
-    _want(mask, torch.int64, "mask")
+    if parents.dim() != 2:
+        raise ValueError("parents is int32 [B, N]")
     B, N = parents.shape
+    _want(mask, torch.int64, "mask", (B, N))
+    if depth is not None:
+        _want(depth, torch.int32, "depth", (B, N))
+    _want(status, torch.int32, "status", (B,))
     _check(_mask(_ptr(parents), B, N, _ptr(mask), _ptr(depth), _ptr(status), _stream(stream)),
            "tree_mask_build")
 
@@ -147,19 +158,34 @@ def tree_verify_attention_kernels(B, N, Hq, Hkv, d, max_blocks_per_seq, block_si
     return int(_attn_nk(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size, dt, workspace_bytes))
 
 
+def _attention_args(q, k_cache, v_cache, block_table, prefix_lens, mask, out, status):
+    """Shape and dtype checks shared by both attention entry points."""
+    if q.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("q is [B,N,Hq,d] and the caches [num_blocks,Hkv,block_size,d]")
+    B, N, Hq, d = q.shape
+    num_blocks, Hkv, bs, d2 = k_cache.shape
+    if d2 != d:
+        raise ValueError("q and the caches disagree on the head size")
+    dt = _dtype_code(q)
+    _want(k_cache, q.dtype, "k_cache")
+    _want(v_cache, q.dtype, "v_cache", k_cache.shape)
+    _want(out, q.dtype, "out", q.shape)
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table is int32 [B, max_blocks_per_seq]")
+    _want(block_table, torch.int32, "block_table")
+    _want(prefix_lens, torch.int32, "prefix_lens", (B,))
+    _want(mask, torch.int64, "mask", (B, N))
+    _want(status, torch.int32, "status", (B,))
+    return B, N, Hq, Hkv, d, bs, num_blocks, dt
+
+
 def tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, mask, out, status,
                           workspace=None, *, scale: float = 0.0, stream=None) -> None:
     """q [B,N,Hq,d]; caches [num_blocks,Hkv,bs,d]; block_table int32 [B,max_blocks];
     prefix_lens int32 [B]; mask int64 [B,N]; out like q; status int32 [B];
     workspace uint8 tensor (zero-filled before first use)."""
-    B, N, Hq, d = q.shape
-    num_blocks, Hkv, bs, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
-        raise ValueError("shape mismatch")
-    for t, n in ((block_table, "block_table"), (prefix_lens, "prefix_lens"), (status, "status")):
-        _want(t, torch.int32, n)
-    _want(mask, torch.int64, "mask")
-    dt = _dt(q)
+    B, N, Hq, Hkv, d, bs, num_blocks, dt = _attention_args(q, k_cache, v_cache, block_table,
+                                                           prefix_lens, mask, out, status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
                  _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs, num_blocks, dt, scale,
@@ -173,15 +199,15 @@ def tree_verify_attention_noalloc_capacity() -> int:
 
 def tree_verify_attention_noalloc(q, k_cache, v_cache, block_table, prefix_lens, mask, out,
                                   status, *, scale: float = 0.0, stream=None) -> None:
-    """tree_verify_attention without a caller workspace: scratch comes from a
-    fixed array inside the library (see the C header for the constraints)."""
-    B, N, Hq, d = q.shape
-    num_blocks, Hkv, bs, d2 = k_cache.shape
-    if d2 != d or v_cache.shape != k_cache.shape or out.shape != q.shape:
-        raise ValueError("shape mismatch")
+    """tree_verify_attention for callers that cannot hand the library a
+    workspace: the scratch is a fixed array inside the library, shared by
+    every call on a device (overlapping calls race on it; the C header gives
+    the size limit)."""
+    B, N, Hq, Hkv, d, bs, num_blocks, dt = _attention_args(q, k_cache, v_cache, block_table,
+                                                           prefix_lens, mask, out, status)
     _check(_attn_na(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                     block_table.shape[1], _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs,
-                    num_blocks, _dt(q), scale, _ptr(out), _ptr(status), _stream(stream)),
+                    num_blocks, dt, scale, _ptr(out), _ptr(status), _stream(stream)),
            "tree_verify_attention_noalloc")
 
 
@@ -192,10 +218,22 @@ def tree_accept_workspace(mode, B, N, V) -> int:
 def tree_accept(mode, parents, draft_tokens, target, draft_probs, accept_len, path, out_tokens,
                 status, *, seed: int = 0, offset: int = 0, workspace=None, stream=None) -> None:
     """Greedy (target = logits) or stochastic chain (target = p, draft_probs = q) acceptance."""
+    if target.dim() != 3:
+        raise ValueError("target is float32 [B, N, V]")
     B, N, V = target.shape
     _want(target, torch.float32, "target")
     if draft_probs is not None:
-        _want(draft_probs, torch.float32, "draft_probs")
+        _want(draft_probs, torch.float32, "draft_probs", target.shape)
+    _want(parents, torch.int32, "parents", (B, N))
+    _want(draft_tokens, torch.int32, "draft_tokens", (B, N))
+    if path.dim() != 2 or path.shape[0] != B:
+        raise ValueError("path is int32 [B, max_path]")
+    _want(path, torch.int32, "path")
+    _want(out_tokens, torch.int32, "out_tokens", path.shape)
+    _want(accept_len, torch.int32, "accept_len", (B,))
+    _want(status, torch.int32, "status", (B,))
+    if workspace is not None:
+        _want(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_acc(mode, _ptr(parents), _ptr(draft_tokens), _ptr(target), _ptr(draft_probs), B, N,
                 V, seed, offset, _ptr(accept_len), _ptr(path), _ptr(out_tokens), path.shape[1],
@@ -206,11 +244,26 @@ def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_le
                    rope_theta: float = 0.0, stream=None) -> None:
     """k_new / v_new [B,N,Hkv,d]; caches [num_blocks,Hkv,bs,d]; depth int32 [B,N]
     (needed when rope_theta > 0); status int32 [B]."""
+    if k_new.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError("k_new is [B,N,Hkv,d] and the caches [num_blocks,Hkv,block_size,d]")
     B, N, Hkv, d = k_new.shape
-    num_blocks, _, bs, _ = k_cache.shape
+    num_blocks, Hkv2, bs, d2 = k_cache.shape
+    if (Hkv2, d2) != (Hkv, d):
+        raise ValueError("k_new and the caches disagree on Hkv or the head size")
+    _dtype_code(k_cache)
+    _want(k_new, k_cache.dtype, "k_new")
+    _want(v_new, k_cache.dtype, "v_new", k_new.shape)
+    _want(v_cache, k_cache.dtype, "v_cache", k_cache.shape)
+    if depth is not None:
+        _want(depth, torch.int32, "depth", (B, N))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table is int32 [B, max_blocks_per_seq]")
+    _want(block_table, torch.int32, "block_table")
+    _want(prefix_lens, torch.int32, "prefix_lens", (B,))
+    _want(status, torch.int32, "status", (B,))
     _check(_append(_ptr(k_new), _ptr(v_new), _ptr(depth), B, N, Hkv, d, float(rope_theta),
                    _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-                   _ptr(prefix_lens), bs, num_blocks, _dt(k_cache), _ptr(status), _stream(stream)),
+                   _ptr(prefix_lens), bs, num_blocks, _dtype_code(k_cache), _ptr(status), _stream(stream)),
            "tree_kv_append")
 
 
@@ -220,16 +273,33 @@ def kv_compact(k_cache, v_cache, block_table, prefix_lens, path, accept_len, new
     """Caches [num_layers*][num_blocks,Hkv,bs,d] (layers back to back, ``layer_stride``
     elements apart); path int32 [B,max_path]; accept_len int32 [B]."""
     num_blocks, Hkv, bs, d = k_cache.shape[-4:]
+    if path.dim() != 2:
+        raise ValueError("path is int32 [B, max_path]")
     B, max_path = path.shape
+    _dtype_code(k_cache)
+    _want(v_cache, k_cache.dtype, "v_cache", k_cache.shape)
+    _want(path, torch.int32, "path")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table is int32 [B, max_blocks_per_seq]")
+    _want(block_table, torch.int32, "block_table")
+    for t, n in ((prefix_lens, "prefix_lens"), (accept_len, "accept_len"),
+                 (new_lens, "new_lens"), (status, "status")):
+        _want(t, torch.int32, n, (B,))
+    for t, n in ((src_slots, "src_slots"), (dst_slots, "dst_slots")):
+        if t is not None:
+            _want(t, torch.int64, n, (B, max_path))
+    if num_layers < 1 or (num_layers > 1 and
+                          k_cache.numel() < (num_layers - 1) * layer_stride + num_blocks * Hkv * bs * d):
+        raise ValueError("the caches hold fewer than num_layers layers at layer_stride")
     _check(_compact(_ptr(k_cache), _ptr(v_cache), num_layers, layer_stride, _ptr(block_table),
                     block_table.shape[1], _ptr(prefix_lens), _ptr(path), _ptr(accept_len),
-                    max_path, B, Hkv, d, bs, num_blocks, _dt(k_cache), _ptr(new_lens),
+                    max_path, B, Hkv, d, bs, num_blocks, _dtype_code(k_cache), _ptr(new_lens),
                     _ptr(src_slots), _ptr(dst_slots), _ptr(status), _stream(stream)),
            "kv_compact")
 
 
 def draft_tree_workspace(B, topk, layers) -> int:
-    return int(_dt_ws(B, topk, layers))
+    return int(_draft_ws(B, topk, layers))
 
 
 def draft_tree_expand(logits, layer, layers, status, workspace, *, topk, root_tokens=None,
@@ -239,18 +309,22 @@ def draft_tree_expand(logits, layer, layers, status, workspace, *, topk, root_to
     topk); root_tokens int32 [B] (layer 0); front_tokens / front_src int32
     [B, topk]; on the last layer parents / tokens int32 [B, N] and scores
     float32 [B, N]; workspace uint8 (zero-filled before the first call)."""
-    B, F, V = logits.shape
     _want(logits, torch.float32, "logits")
-    _want(status, torch.int32, "status")
-    for t, n in ((root_tokens, "root_tokens"), (front_tokens, "front_tokens"),
-                 (front_src, "front_src"), (parents, "parents"), (tokens, "tokens")):
+    if logits.dim() != 3:
+        raise ValueError("logits is float32 [B, F, V]")
+    B, F, V = logits.shape
+    _want(status, torch.int32, "status", (B,))
+    for t, n, shp in ((root_tokens, "root_tokens", (B,)), (front_tokens, "front_tokens", (B, topk)),
+                      (front_src, "front_src", (B, topk)), (parents, "parents", (B, N)),
+                      (tokens, "tokens", (B, N))):
         if t is not None:
-            _want(t, torch.int32, n)
+            _want(t, torch.int32, n, shp)
     if scores is not None:
-        _want(scores, torch.float32, "scores")
+        _want(scores, torch.float32, "scores", (B, N))
+    _want(workspace, torch.uint8, "workspace")
     if F != (1 if layer == 0 else topk):
         raise ValueError(f"layer {layer} takes {1 if layer == 0 else topk} rows per sequence")
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(_dt(_ptr(logits), _ptr(root_tokens), B, V, topk, layer, layers, N, _ptr(front_tokens),
+    _check(_draft_expand(_ptr(logits), _ptr(root_tokens), B, V, topk, layer, layers, N, _ptr(front_tokens),
                _ptr(front_src), _ptr(parents), _ptr(tokens), _ptr(scores), _ptr(status),
                _ptr(workspace), ws_bytes, _stream(stream)), "draft_tree_expand")

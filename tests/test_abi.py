@@ -149,6 +149,114 @@ def test_draft_tree_binding_checks_need_no_gpu(lib):
                              root_tokens=torch.zeros(2, dtype=torch.int32))
 
 
+def declared_arity():
+    """Parameter count of every function include/treeverify.h declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(([^;{}]*?)\)\s*;", text):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_handles_match_the_header(lib):
+    """Each module-level ctypes handle of the binding is the C symbol it is
+    named after and carries the header's parameter count: a later rebinding of
+    a handle's name (a helper of the same name) fails here, on the CPU."""
+    pytest.importorskip("torch")
+    import eagle_speculative_decoding_parent_gb300 as tv
+    arity = declared_arity()
+    handles = {n: getattr(tv, n) for n in dir(tv)
+               if isinstance(getattr(tv, n), ctypes._CFuncPtr)}
+    bound = {}
+    for name, fn in handles.items():
+        assert fn.__name__ in arity, (name, fn.__name__)
+        assert len(fn.argtypes) == arity[fn.__name__], (name, fn.__name__, len(fn.argtypes))
+        bound[fn.__name__] = name
+    # every entry point the binding exports has its handle
+    for public in ("tree_mask_build", "tree_verify_attention", "tree_verify_attention_noalloc",
+                   "tree_accept", "kv_compact", "tree_kv_append", "draft_tree_expand",
+                   "draft_tree_workspace", "tree_verify_attention_workspace",
+                   "tree_accept_workspace", "tree_verify_attention_kernels"):
+        assert public in bound, public
+    assert tv._draft_expand.__name__ == "draft_tree_expand" and len(tv._draft_expand.argtypes) == 17
+
+
+def _attn_host_tensors(torch, dtype=None, mask_dtype=None, status_dtype=None, table_dtype=None,
+                       kv_dtype=None):
+    B, N, Hq, Hkv, d, nb, bs = 2, 3, 4, 2, 64, 6, 16
+    dtype = dtype or torch.bfloat16
+    q = torch.zeros(B, N, Hq, d, dtype=dtype)
+    k = torch.zeros(nb, Hkv, bs, d, dtype=kv_dtype or dtype)
+    v = torch.zeros(nb, Hkv, bs, d, dtype=kv_dtype or dtype)
+    bt = torch.zeros(B, 3, dtype=table_dtype or torch.int32)
+    P = torch.zeros(B, dtype=torch.int32)
+    mask = torch.zeros(B, N, dtype=mask_dtype or torch.int64)
+    out = torch.zeros_like(q)
+    st = torch.zeros(B, dtype=status_dtype or torch.int32)
+    return q, k, v, bt, P, mask, out, st
+
+
+@pytest.mark.parametrize("entry", ["tree_verify_attention", "tree_verify_attention_noalloc"])
+def test_attention_bindings_check_dtypes_and_shapes(lib, entry):
+    """Both attention entry points reject, before any pointer reaches the
+    library, buffers whose element type or shape would make the kernels index
+    past their end (an int32 mask read as 64-bit words, an int8 status written
+    as int32, caches of another type than q)."""
+    torch = pytest.importorskip("torch")
+    import eagle_speculative_decoding_parent_gb300 as tv
+    fn = getattr(tv, entry)
+    for kw, exc in ((dict(mask_dtype=torch.int32), TypeError),
+                    (dict(status_dtype=torch.int8), TypeError),
+                    (dict(table_dtype=torch.int64), TypeError),
+                    (dict(kv_dtype=torch.float16), TypeError),
+                    (dict(kv_dtype=torch.float32), TypeError),
+                    (dict(dtype=torch.float16), TypeError)):
+        with pytest.raises(exc):
+            fn(*_attn_host_tensors(torch, **kw))
+    q, k, v, bt, P, mask, out, st = _attn_host_tensors(torch)
+    with pytest.raises(ValueError):
+        fn(q, k, v, bt, P, mask[:, :2], out, st)          # mask narrower than N
+    with pytest.raises(ValueError):
+        fn(q, k, v, bt, P, mask, out, st[:1])             # status shorter than B
+    with pytest.raises(ValueError):
+        fn(q, k, v, bt[:1], P, mask, out, st)             # block table for fewer sequences
+    with pytest.raises(ValueError, match="CUDA device"):
+        fn(q, k, v, bt, P, mask, out, st)                 # well-formed, but host memory
+
+
+def test_accept_and_compact_bindings_check_dtypes(lib):
+    torch = pytest.importorskip("torch")
+    import eagle_speculative_decoding_parent_gb300 as tv
+    B, N, V, mp = 2, 4, 10, 3
+    i32 = lambda *s: torch.zeros(*s, dtype=torch.int32)
+    args = lambda **o: dict(dict(mode=tv.GREEDY, parents=i32(B, N), draft_tokens=i32(B, N),
+                                 target=torch.zeros(B, N, V), draft_probs=None,
+                                 accept_len=i32(B), path=i32(B, mp), out_tokens=i32(B, mp),
+                                 status=i32(B)), **o)
+    with pytest.raises(TypeError):
+        tv.tree_accept(**args(parents=torch.zeros(B, N, dtype=torch.int64)))
+    with pytest.raises(ValueError):
+        tv.tree_accept(**args(out_tokens=i32(B, mp + 1)))
+    with pytest.raises(TypeError):
+        tv.tree_accept(**args(status=torch.zeros(B, dtype=torch.int8)))
+    with pytest.raises(ValueError, match="CUDA device"):
+        tv.tree_accept(**args())
+    k = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
+    cargs = lambda **o: dict(dict(k_cache=k, v_cache=k.clone(), block_table=i32(B, 2),
+                                  prefix_lens=i32(B), path=i32(B, mp), accept_len=i32(B),
+                                  new_lens=i32(B), status=i32(B)), **o)
+    with pytest.raises(TypeError):
+        tv.kv_compact(**cargs(v_cache=k.float()))
+    with pytest.raises(TypeError):
+        tv.kv_compact(**cargs(src_slots=i32(B, mp)))
+    with pytest.raises(ValueError):
+        tv.kv_compact(**cargs(num_layers=2, layer_stride=k.numel()))
+    with pytest.raises(ValueError, match="CUDA device"):
+        tv.kv_compact(**cargs())
+
+
 @pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
 def test_header_is_plain_c_and_cpp(lang, std, tmp_path):
     """include/treeverify.h compiles on its own as C99 and as C++11, with no
