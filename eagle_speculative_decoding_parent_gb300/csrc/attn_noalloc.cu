@@ -74,7 +74,10 @@ extern "C" tv_status tree_verify_attention_noalloc(
         if (zero > 0 && cudaMemsetAsync(scratch, 0, zero, (cudaStream_t)stream) != cudaSuccess)
             return TV_ERR_CUDA;
     }
+    // The workspace size passed on is exactly `need`, the size the workspace
+    // query gives for this shape, so this call takes the same schedule as a
+    // tree_verify_attention call whose caller sized its workspace by that query.
     return tree_verify_attention(q, k_cache, v_cache, block_table, max_blocks_per_seq,
                                  prefix_lens, mask, B, N, Hq, Hkv, d, block_size, num_blocks, dt,
-                                 scale, out, status, scratch, need > 0 ? kScratchBytes : 0, stream);
+                                 scale, out, status, scratch, need, stream);
 }

@@ -330,7 +330,10 @@ tv_status draft_tree_expand(const float* logits, const int32_t* root_tokens, int
  * all of HBM for its own pools up front and does not allocate while decoding,
  * or a plugin host that gives its plugins no allocator.  This call computes
  * exactly what tree_verify_attention computes (same arguments, minus the
- * workspace) but takes its scratch from a fixed array inside the library:
+ * workspace) but takes its scratch from a fixed array inside the library,
+ * and picks the schedule a tree_verify_attention call would pick with a
+ * workspace of exactly tree_verify_attention_workspace(...) bytes, so the
+ * two give bit-identical outputs.  The array is
  * TV_NOALLOC_SCRATCH_BYTES of device memory that every GPU loading the
  * library holds until the process exits.  It never calls cudaMalloc,
  * cudaFree or any allocating routine.
