@@ -734,10 +734,12 @@ int64_t orc_sample_weights_u32(const uint64_t* w, int64_t V, uint32_t x) {
  *   - a node's draft row is log-softmax'ed; its candidate children are the k
  *     tokens with the largest logits (ties: lowest token id);
  *   - a node's score is its path's cumulative draft log-probability,
- *     score(child) = score(parent) + (logit - logsumexp(row)), the logsumexp
- *     in double rounded to binary32 and both operations in binary32: the
- *     pages fix no precision, so the ranking decisions are taken in the
- *     library's (binary32);
+ *     score(child) = score(parent) + (logit - logsumexp(row)).  Which nodes
+ *     are kept, and in which order, is an integer result decided by
+ *     comparing these scores; the pages fix no precision for it, so the
+ *     scores are formed in binary32, the precision the draft logits come
+ *     in: the logsumexp accumulated in double and rounded once, then one
+ *     binary32 subtraction and one binary32 addition;
  *   - nodes are numbered in creation order: frontier node f's children are
  *     created f-major, child rank j minor;
  *   - the next frontier is the k best nodes created in this layer, by

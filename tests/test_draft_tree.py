@@ -2,10 +2,11 @@
 against the oracle, layer by layer, on seeded synthetic draft logits.
 
 The top-k of every row is decided by exact comparisons of fp32 logits on both
-sides, so it must match bit for bit.  Scores are cumulative log-probabilities:
-fp32 on the GPU (logsumexp reduced in the kernel's order, measured within
-about 1e-6 of fp64 per row at these vocabulary sizes), fp64 in the oracle;
-they must agree within SCORE_TOL.  The frontier and the final cut rank those
+sides, so it must match bit for bit.  Scores are cumulative log-probabilities
+formed in binary32 on both sides; the logsumexp they subtract is reduced in
+binary32 in the kernel's order and accumulated in double then rounded once in
+the oracle (the two agree within about 1e-6 per row at these vocabulary
+sizes), so the scores must agree within SCORE_TOL.  The frontier and the final cut rank those
 scores, so a sequence is compared exactly (frontiers, parents, tokens) when
 every ranking gap the oracle saw is at least EXACT_MARGIN; a sequence with a
 closer call may legitimately break it the other way, and for it the test
@@ -14,8 +15,6 @@ match the oracle's.  Rows are indexed by frontier position, so such a swap
 changes parent scores by less than the gap and leaves the score multiset
 within tolerance.
 
-This file is collected after every other test file: it covers the newest
-kernel, so a run stopping at its first failure has already run the rest.
 """
 import numpy as np
 import pytest

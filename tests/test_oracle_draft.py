@@ -8,8 +8,9 @@ high-probability ones, prune the rest); the oracle fills it in EAGLE-2 style
 N - 1 best nodes kept, breadth-first labels).  These tests check it against
 things fixed independently of its code:
 
-Scores are ranked in binary32 (the library's precision; the pages fix none),
-so they are compared with the double-precision recomputations within 5e-5.
+Scores are formed in binary32, the precision of the draft logits (the pages
+fix none for the ranking, an integer result decided by comparing scores), so
+they are compared with the double-precision recomputations within 5e-5.
 
 * exhaustive enumeration: when k >= N - 1 no pruning step can drop a node of
   the best N - 1 root paths (each of them has fewer than k better nodes at its
