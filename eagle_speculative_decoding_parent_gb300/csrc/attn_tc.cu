@@ -17,14 +17,21 @@
 // A row tile holds npt = floor(128 / G) whole nodes (all G query heads of the
 // kv head for each), rows r = node * G + head, so one TMA box loads it.
 //
-// CTA roles (256 threads, one CTA per SM)
+// CTA roles (288 threads, one CTA per SM)
 //   warp 0   producer of pages 0-1 of each 64-key K/V tile; warp 2 loads
 //            pages 2-3.  A 16-key page is two K boxes (one per 64-column half)
 //            and one V box holding both halves; the ring has 5 stages (4 when a
-//            cluster splits the group).
-//            Warp 0 of rank 0 also hands out the work items; warp 2 allocates /
-//            frees 512 tensor-memory columns: S double buffer (2 x 64), O (128),
-//            P (2 x 32).
+//            cluster splits the group).  Neither producer ever waits for data:
+//            the rows of a group's last, partial tile past the sequence end are
+//            zeroed in V by the PV issuer just before its product.
+//            Warp 2 allocates / frees 512 tensor-memory columns: S double buffer
+//            (2 x 64), O (128), P (2 x 32).
+//   warp 8   work items (cluster schedule, rank 0): takes the next group from
+//            the counter, checks its sequence's block table and resolves each
+//            rank's first 32 pages into cache rows, one group ahead of the
+//            producers, so a new group's copies start without a global-memory
+//            round trip.  Under the balanced split the pieces are listed in the
+//            prologue and warp 0 hands them out.
 //   warp 1   S issuer: loads each group's Q tile (3-D TMA box) once the
 //            previous group's S products are done with it, so the K/V stream
 //            runs on across groups; S = Q K^T into tensor memory (M=128, N=64,
@@ -59,8 +66,13 @@ constexpr int KT = 64;        // keys per tile
 constexpr int STAGES = 5;           // K/V ring depth when a CTA owns whole groups
 constexpr int STAGES_CLUSTER = 4;   // with a cluster split the fifth stage holds the merge rows
 constexpr int GQ = 4;
-constexpr int THREADS = 256;
-constexpr int SOFTMAX_WARP0 = 4;
+constexpr int THREADS = 288;
+constexpr int SOFTMAX_WARP0 = 4;  // softmax warps 4-7
+constexpr int FETCH_WARP = 8;
+// Cluster schedule: the next group is claimed when this many key tiles of the
+// current one are left to issue (enough to hide the claim and the block-table
+// checks, late enough to keep the longest-first balance of the counter).
+constexpr int FETCH_LEAD = 6;
 constexpr int MAX_CS = 8;
 constexpr int D = 128;
 constexpr uint32_t TMEM_COLS = 512;
@@ -91,7 +103,8 @@ constexpr int OFF_GQ4 = OFF_CUM + (LPT_MAX + 1) * 8 + 8;  // queue slots [GQ] x 
 constexpr int MAXI = 64;                               // balanced split: pieces listed up front
 constexpr int OFF_ITEMS = OFF_GQ4 + GQ * 16;           // [MAXI] x (word, first tile, end tile, bad)
 constexpr int OFF_NITEMS = OFF_ITEMS + MAXI * 16;
-constexpr int SMEM_BYTES = OFF_NITEMS + 16 + 1024;     // + alignment slack
+constexpr int OFF_WIN = OFF_NITEMS + 16;               // [GQ][32] first-window cache rows
+constexpr int SMEM_BYTES = OFF_WIN + GQ * 32 * 4 + 1024;  // + alignment slack
 static_assert(OFF_CUM % 8 == 0, "int64 prefix sums");
 static_assert(OFF_ITEMS % 16 == 0 && OFF_GQ4 % 16 == 0, "int4 slots");
 // Balanced split: cost of starting a piece (Q tile, pipeline fill and drain,
@@ -251,8 +264,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     uint64_t* pfull = sfree + 2;              // [2]
     uint64_t* pfree = pfull + 2;              // [2] PV product of tile t done (by t & 1)
     uint64_t* ofree = pfree + 2;
-    uint64_t* tailb = ofree + 1;
-    uint64_t* gq_full = tailb + 1;            // [GQ]
+    uint64_t* ptake = ofree + 1;              // producer took item k (phase k & 1)
+    uint64_t* gq_full = ptake + 1;            // [GQ]
     uint64_t* gq_empty = gq_full + GQ;        // [GQ]
     uint64_t* xready = gq_empty + GQ;
     uint64_t* xfree = xready + 1;
@@ -283,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_init(&pfree[i], 1);
         }
         mbar_init(ofree, 4);
-        mbar_init(tailb, 2);
+        mbar_init(ptake, 1);
         for (int s = 0; s < GQ; ++s) {
             mbar_init(&gq_full[s], 1);
             mbar_init(&gq_empty[s], cs * 8);      // 2 producers, 2 MMA issuers, 4 softmax warps
@@ -311,6 +324,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int4* items = reinterpret_cast<int4*>(smem + OFF_ITEMS);  // word, first tile, end tile, bad
     int* n_items = reinterpret_cast<int*>(smem + OFF_NITEMS);
     int* items_more = n_items + 1;
+    // cluster schedule: per queue slot, lane l's page l of the first window as a cache row
+    int* win0 = reinterpret_cast<int*>(smem + OFF_WIN);
     // balanced split: this CTA's run [x_lo, x_hi) of the run space and its row tile
     int64_t U = 0, L = 0, x_lo = 0, x_hi = 0;
     int qt_me = 0;
@@ -442,58 +457,86 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         __syncthreads();
     }
 
-    // work item k of this CTA (all roles walk the same sequence)
-    // (the fetcher is a whole warp: it also validates the group's sequence)
-    auto next_group = [&](uint32_t k, bool fetcher) -> Item {
+    // Work item k: the fetching warp publishes it into every cluster rank's
+    // queue slot (fetch_item), every role reads it from its own (take_item).
+    // The fetcher is a whole warp: it also validates the group's sequence and,
+    // under the cluster schedule, resolves each rank's first window of 32 pages
+    // into cache rows (win0).  Returns the group index (>= p.groups: the end).
+    auto fetch_item = [&](uint32_t k) -> int {
         const int slot = k % GQ;
-        if (fetcher) {
-            int gi = p.groups, tlo = 0, thi = 0, word = p.groups;
-            const bool free_slot = __all_sync(
-                0xffffffffu, lane != 0 || mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u));
-            if (!free_slot) {
-                // timed out: hand out the end marker
-            } else if (SPLIT && (int)k < *n_items) {
-                word = items[k].x;  // listed and checked in the prologue
-                tlo = items[k].y;
-                thi = items[k].z;
+        int gi = p.groups, tlo = 0, thi = 0, word = p.groups;
+        const bool free_slot = __all_sync(
+            0xffffffffu, lane != 0 || mbar_wait_cluster(&gq_empty[slot], ((k / GQ) & 1u) ^ 1u));
+        if (!free_slot) {
+            // timed out: hand out the end marker
+        } else if (SPLIT && (int)k < *n_items) {
+            word = items[k].x;  // listed and checked in the prologue
+            gi = word & (GROUP_BAD - 1);
+            tlo = items[k].y;
+            thi = items[k].z;
+        } else {
+            if constexpr (SPLIT) {
+                if (!*items_more) gi = p.groups;
+                else split_next(gi, tlo, thi);
             } else {
-                if constexpr (SPLIT) {
-                    if (!*items_more) gi = p.groups;
-                    else split_next(gi, tlo, thi);
-                } else {
-                    // the first group of every cluster is its cluster index; later ones
-                    // come from the counter, after the clusters' first groups
-                    const int nclusters = (int)(gridDim.x / cs);
-                    if (lane == 0)
-                        gi = (k == 0) ? (int)(blockIdx.x / cs)
-                                      : nclusters + atomicAdd(&p.sched[0], 1);
-                    gi = __shfl_sync(0xffffffffu, gi, 0);
-                }
-                word = gi;
-                if (gi < p.groups) {
-                    const int b = group_seq(p, order, gi);
-                    if (!seq_ok_warp(p, b, lens ? lens[b] : p.prefix_lens[b])) word |= GROUP_BAD;
-                }
+                // the first group of every cluster is its cluster index; later ones
+                // come from the counter, after the clusters' first groups
+                const int nclusters = (int)(gridDim.x / cs);
+                if (lane == 0)
+                    gi = (k == 0) ? (int)(blockIdx.x / cs) : nclusters + atomicAdd(&p.sched[0], 1);
+                gi = __shfl_sync(0xffffffffu, gi, 0);
             }
-            if (lane == 0) {
-                gq4[slot].y = tlo;  // balanced split only: no cluster peers
-                gq4[slot].z = thi;
-                for (uint32_t r = 0; r < cs; ++r) {
-                    remote_st_u32(&gq4[slot].x, r, word);
-                    remote_arrive(&gq_full[slot], r);
+            word = gi;
+            if (gi < p.groups) {
+                const int b = group_seq(p, order, gi);
+                const int P = lens ? lens[b] : p.prefix_lens[b];
+                if (!seq_ok_warp(p, b, P)) {
+                    word |= GROUP_BAD;
+                } else if (!SPLIT) {
+                    // each rank's first window: page `lane` of its share of the keys
+                    const int g = (gi / p.QT) % p.Hkv, Lg = P + p.N, T = (Lg + KT - 1) / KT;
+                    for (uint32_t r = 0; r < cs; ++r) {
+                        const int tk = ((int)((int64_t)T * r / cs) * (KT / 16) + lane) * 16;
+                        int y = 0;
+                        if (tk < Lg)
+                            y = (__ldg(p.table + (int64_t)b * p.max_blocks + tk / p.bs) * p.Hkv + g) * p.bs +
+                                tk % p.bs;
+                        remote_st_u32(&win0[slot * 32 + lane], r, y);
+                    }
+                    asm volatile("fence.acq_rel.cluster;" ::: "memory");
                 }
             }
         }
+        __syncwarp();
+        if (lane == 0) {
+            gq4[slot].y = tlo;  // balanced split only: no cluster peers
+            gq4[slot].z = thi;
+            for (uint32_t r = 0; r < cs; ++r) {
+                remote_st_u32(&gq4[slot].x, r, word);
+                remote_arrive(&gq_full[slot], r);
+            }
+        }
+        return gi;
+    };
+    // y0 (nullable): this lane's page of the first window, as a cache row
+    auto take_item = [&](uint32_t k, int* y0) -> Item {
+        const int slot = k % GQ;
         const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&gq_full[slot], (k / GQ) & 1u));
         const int4 v = lds_v4_volatile(&gq4[slot]);
         Item it;
         it.word = got ? v.x : p.groups;
         it.t_lo = v.y;
         it.t_hi = v.z;
+        int dep = got ? v.x : 0;
+        if (y0) {
+            *y0 = *reinterpret_cast<volatile int*>(&win0[slot * 32 + lane]);
+            // the slot may be refilled only after every lane's row was read
+            if (__any_sync(0xffffffffu, *y0 < 0)) dep |= INT_MIN;
+        }
         __syncwarp();
         // "slot read": no release needed, and a release here would wait for the
         // softmax warps' output stores of the previous group
-        if (lane == 0) remote_arrive_relaxed_after(&gq_empty[slot], 0, got ? v.x : 0);
+        if (lane == 0) remote_arrive_relaxed_after(&gq_empty[slot], 0, dep);
         return it;
     };
 
@@ -512,17 +555,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tma_prefetch_desc(&vmap);
         }
         const uint64_t policy = (p.QT == 1) ? l2_policy_evict_first() : l2_policy_evict_normal();
-        uint32_t gt = 0, tail_phase = 0;
+        uint32_t gt = 0;
         bool alive = true;
         // balanced split: block id of page `lane` of listed piece pf_k, loaded one
         // piece ahead
         int pf_blk = 0, pf_k = -1;
         for (uint32_t k = 0; alive; ++k) {
-            const Item it = next_group(k, kprod && rank == 0);
+            int y0 = 0;
+            if (SPLIT && kprod && rank == 0) fetch_item(k);
+            const Item it = take_item(k, SPLIT ? nullptr : &y0);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
-            if (n == 0) continue;
+            // cluster schedule: let the fetch warp claim item k + 1 once FETCH_LEAD
+            // tiles of this one are left to issue (at once for an empty one)
+            const bool signals = !SPLIT && kprod && rank == 0;
+            const int t_signal = max(gr.t_lo, gr.t_hi - FETCH_LEAD);
+            if (n == 0) {
+                if (signals && lane == 0) mbar_arrive(ptake);
+                continue;
+            }
             // cache rows of the group's 16-key pages, 32 pages (8 tiles) per window:
             // lane l holds page l of the current window as a row index, and the
             // block id (loaded 8 tiles ahead) and row-in-block of the next window
@@ -534,8 +586,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 nxt_off = tk % p.bs;
             };
             auto row_of = [&]() -> int { return (nxt_blk * p.Hkv + gr.g) * p.bs + nxt_off; };
-            int win_y = 0;
-            if (gr.t_lo < gr.t_hi) {
+            int win_y = y0;  // cluster schedule: resolved by the fetch warp
+            if (SPLIT && gr.t_lo < gr.t_hi) {
                 if (pf_k == (int)k) {  // loaded while the previous piece streamed
                     nxt_blk = pf_blk;
                     nxt_off = ((gr.t_lo * (KT / 16) + lane) * 16) % p.bs;
@@ -571,15 +623,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     alive = false;
                     break;
                 }
+                if (signals && t == t_signal && lane == 0) mbar_arrive(ptake);
                 const int t0 = t * KT;
                 const int nv = min(KT, gr.L - t0);
                 const int pages = (nv + 15) >> 4;
                 const int mine = max(0, min(KT / 32, pages - pg0));  // this warp's pages
                 const uint32_t bytes = (uint32_t)mine * 16u * D * 2u * 2u;
-                // a partial tile lands on its own barrier: V rows past the end are
-                // zeroed by warp 0 before the stage is published
-                const bool tail = nv < KT;
-                uint64_t* bar = tail ? tailb : &kfull[s];
+                uint64_t* bar = &kfull[s];
                 uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
                 uint8_t* vt = kt + TILE_BYTES;
                 // the window holds every page's cache row; the warp walks its pages with
@@ -601,34 +651,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     win_y = row_of();
                     if (gr.t_lo + (w + 1) * WIN_TILES < gr.t_hi) load_window(w + 1);
                 }
-                if (tail && !kprod) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&kfull[s]);
-                } else if (tail) {
-                    const bool landed = __all_sync(0xffffffffu, mbar_wait(tailb, tail_phase));
-                    tail_phase ^= 1u;
-                    if (!landed) {
-                        if (lane == 0) {
-                            flags[0] = 1;
-                            p.status[gr.b] = TV_ERR_TIMEOUT;
-                        }
-                        alive = false;
-                        break;
-                    }
-                    // rows past the sequence end may hold anything: zero V there (K rows
-                    // are masked); V is [page][half][16 rows][128 bytes]
-                    const int zrows = KT - nv;
-                    for (int e = lane; e < 2 * zrows * 8; e += 32) {
-                        const int hf = e / (zrows * 8);
-                        const int r = nv + (e / 8) % zrows;
-                        const int ch = e % 8;
-                        *reinterpret_cast<uint4*>(vt + (r >> 4) * 4096 + hf * 2048 + (r & 15) * 128 +
-                                                  ch * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();  // the tensor core reads V through the async proxy
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&kfull[s]);
-                }
             }
         }
     } else if (warp == 1) {
@@ -639,7 +661,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (lane == 0) tma_prefetch_desc(&qmap);
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
-            const Item it = next_group(k, false);
+            const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
@@ -687,13 +709,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const uint32_t tO = tmem + TMEM_O;
         bool alive = true;
         for (uint32_t k = 0; alive; ++k) {
-            const Item it = next_group(k, false);
+            const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
             for (int j = 0; j < n; ++j, ++gt) {
                 const int pb = gt & 1, s = gt % nst;
+                const int nv = min(KT, gr.L - (gr.t_lo + j) * KT);
+                if (nv < KT) {
+                    // the group's last tile: V rows past the sequence end may hold
+                    // anything (NaN times a zero weight is NaN), so zero them as soon
+                    // as the tile has landed, while the softmax still works on it
+                    if (!wait_all(&kfull[s], (gt / nst) & 1u)) {
+                        alive = false;
+                        break;
+                    }
+                    uint8_t* vt = smem + OFF_RING + s * 2 * TILE_BYTES + TILE_BYTES;
+                    // V is [page][half][16 rows][128 bytes]: one (row, half) per lane
+                    for (int e = lane; e < 2 * (KT - nv); e += 32) {
+                        const int r = nv + (e >> 1);
+                        uint4* dst = reinterpret_cast<uint4*>(vt + (r >> 4) * 4096 + (e & 1) * 2048 +
+                                                              (r & 15) * 128);
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) dst[ch] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();  // the tensor core reads V through the async proxy
+                    __syncwarp();
+                }
                 if (!wait_all(&pfull[pb], (gt >> 1) & 1u) ||
                     (j == 0 && og > 0 && !wait_all(ofree, (og - 1) & 1u))) {
                     alive = false;
@@ -715,8 +758,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             ++og;
         }
         if (!alive && lane == 0) flags[0] = 1;
-    } else if (warp >= SOFTMAX_WARP0) {
-        // ============================= softmax =============================
+    } else if (warp == FETCH_WARP) {
+        // ===== work items (cluster schedule): one group ahead of the producers =====
+        if (!SPLIT && rank == 0) {
+            for (uint32_t k = 0;; ++k) {
+                if (k > 0 && !__all_sync(0xffffffffu, mbar_wait_sleep(ptake, (k - 1) & 1u))) break;
+                if (fetch_item(k) >= p.groups) break;
+            }
+        }
+    } else {
+        // ======================== softmax (warps 4-7) ========================
         const int row = tid - SOFTMAX_WARP0 * 32;           // tensor-memory lane
         const uint32_t lane_off = (uint32_t)(32 * (warp - SOFTMAX_WARP0)) << 16;
         const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + TMEM_O;
@@ -732,7 +783,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             return __all_sync(0xffffffffu, mbar_wait(&pfree[t & 1u], (t >> 1) & 1u));
         };
         for (uint32_t k = 0;; ++k) {
-            const Item it = next_group(k, false);
+            const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
             const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
             if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
@@ -741,8 +792,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             const int node_l = row / p.G, head = row % p.G;
             const int node = gr.qt * p.npt + node_l;
             const bool valid = (node_l < p.npt) && (node < p.N);
-            const uint64_t nmask = (p.N >= 64) ? ~0ull : ((1ull << p.N) - 1);
-            const uint64_t mk = valid ? (p.mask[(int64_t)gr.b * p.N + node] & nmask) : 0ull;
+            // the node's ancestor bits (bits at or above N are never used: the
+            // visibility word is cut at the sequence end); loaded now, first
+            // needed by the group's last key tile
+            const uint64_t mk = valid ? ldg_nc_u64_early(p.mask + (int64_t)gr.b * p.N + node) : 0ull;
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < n && alive; ++j, ++gt) {
                 const int sb = gt & 1;
@@ -765,16 +818,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sfree[sb]);
+                if (lane == 0) mbar_arrive_relaxed(&sfree[sb]);
                 const int t0 = (gr.t_lo + j) * KT;
                 if (t0 + KT > gr.P) {
+                    // visible keys of this tile as one word: bit c for key t0 + c, the
+                    // prefix (t < P) and the node's ancestors (t = P + a, bit a of mk)
+                    const int sh = gr.P - t0;  // tile bit of the first tree key, > -N
+                    const uint64_t pre = (sh >= KT) ? ~0ull : (sh <= 0 ? 0ull : (1ull << sh) - 1ull);
+                    const uint64_t tree = (sh >= KT) ? 0ull : (sh >= 0 ? mk << sh : mk >> -sh);
+                    const int in_seq = gr.L - t0;  // keys t < L: bit a of mk only for a < N
+                    const uint64_t seq = (in_seq >= KT) ? ~0ull : (1ull << in_seq) - 1ull;
+                    const uint64_t vis = pre | (tree & seq);
 #pragma unroll
-                    for (int c = 0; c < KT; ++c) {
-                        const int t = t0 + c;
-                        const bool vis = (t < gr.P) ||
-                                         (t < gr.L && ((mk >> (t - gr.P)) & 1ull));
-                        sv[c] = vis ? sv[c] : -INFINITY;
-                    }
+                    for (int c = 0; c < KT; ++c) sv[c] = ((vis >> c) & 1ull) ? sv[c] : -INFINITY;
                 }
                 const float csc = p.scale_log2;
                 // row maximum of the raw scores (four chains of three-input maxima); the
@@ -841,7 +897,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&pfull[pb]);
+                if (lane == 0) mbar_arrive_relaxed(&pfull[pb]);
             }
             if (!alive) break;
             // ---- epilogue: O / l
@@ -916,7 +972,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (n > 0) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ofree);  // O may be overwritten by the next group
+                if (lane == 0) mbar_arrive_relaxed(ofree);  // O may be overwritten by the next group
             }
             if (gr.whole) continue;
             if (spiece) {

@@ -76,6 +76,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Arrive without release semantics.  A release arrive first waits until every
+// earlier global store of the thread is acknowledged (a microsecond or more
+// under load); barriers that only hand tensor-memory buffers between warps
+// need no such ordering: the tcgen05 wait::ld / wait::st and the tcgen05
+// thread-sync fences on both sides order those accesses.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// 8-byte global load through the read-only path, issued where it is written:
+// the compiler may not sink it towards its first use, so a value loaded at the
+// start of a long loop and first needed near its end costs no wait there.
+__device__ __forceinline__ uint64_t ldg_nc_u64_early(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -92,6 +109,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > TV_WAIT_NS) return false;
+    }
+    return true;
+}
+
+// The same bounded wait for a warp that has nothing else to do for a long time
+// (microseconds): each poll lets the thread be suspended for up to 20 us until
+// the phase completes, so it takes no issue slots from the warps that share its
+// scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity)) {
         if (globaltimer_ns() - t0 > TV_WAIT_NS) return false;
     }
     return true;
