@@ -20,7 +20,8 @@
 // CTA roles (288 threads, one CTA per SM)
 //   warp 0   producer of pages 0-1 of each 64-key K/V tile; warp 2 loads
 //            pages 2-3.  A 16-key page is two K boxes (one per 64-column half)
-//            and one V box holding both halves; the ring has 5 stages (4 when a
+//            and one V box holding both halves; a warp's six copies of a tile are
+//            issued by six lanes at once.  The ring has 5 stages (4 when a
 //            cluster splits the group).  Neither producer ever waits for data:
 //            the rows of a group's last, partial tile past the sequence end are
 //            zeroed in V by the PV issuer just before its product.
@@ -632,19 +633,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 uint64_t* bar = &kfull[s];
                 uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
                 uint8_t* vt = kt + TILE_BYTES;
-                // the window holds every page's cache row; the warp walks its pages with
-                // that row broadcast and one elected lane issues the byte count and copies
+                // the window holds every page's cache row.  One elected lane posts the
+                // byte count, then lanes 0-5 issue the warp's six copies at once: lane
+                // 3 jj + c copies page pg0 + jj, c = 0 / 1 the K halves, c = 2 its V
                 mbar_arrive_expect_tx_elect(bar, bytes);
-#pragma unroll
-                for (int jj = 0; jj < KT / 32; ++jj) {
+                {
+                    const int jj = lane / 3, c = lane - 3 * jj;
                     const int j = pg0 + jj;
                     const int y = __shfl_sync(0xffffffffu, win_y,
                                               ((t - gr.t_lo) % WIN_TILES) * (KT / 16) + j);
-                    if (j < pages) {
-                        tma_load_2d_elect(kt + j * 2048, &kmap, bar, 0, y, policy);
-                        tma_load_2d_elect(kt + KT * 128 + j * 2048, &kmap, bar, 64, y, policy);
-                        tma_load_3d_elect(vt + j * 4096, &vmap, bar, 0, y, 0, policy);
+                    if (lane < 3 * (KT / 32) && j < pages) {
+                        if (c < 2) tma_load_2d(kt + c * (KT * 128) + j * 2048, &kmap, bar, c * 64, y, policy);
+                        else tma_load_3d_hint(vt + j * 4096, &vmap, bar, 0, y, 0, policy);
                     }
+                    __syncwarp();
                 }
                 if ((t - gr.t_lo) % WIN_TILES == WIN_TILES - 1 && t + 1 < gr.t_hi) {
                     const int w = (t - gr.t_lo) / WIN_TILES + 1;   // window of tile t + 1
