@@ -19,9 +19,10 @@
 //
 // CTA roles (288 threads, one CTA per SM)
 //   warp 0   producer of pages 0-1 of each 64-key K/V tile; warp 2 loads
-//            pages 2-3.  A 16-key page is two K boxes (one per 64-column half)
-//            and one V box holding both halves; a warp's six copies of a tile are
-//            issued by six lanes at once.  The ring has 5 stages (4 when a
+//            pages 2-3.  A 16-key page is one K box ([row group][half][8 rows]
+//            [128 B], so the 8-key groups of a tile are 2 KB apart for the S
+//            product) and one V box ([half][16 rows][128 B]); a warp's four copies
+//            of a tile are issued by four lanes at once.  The ring has 5 stages (4 when a
 //            cluster splits the group).  Neither producer ever waits for data:
 //            the rows of a group's last, partial tile past the sequence end are
 //            zeroed in V by the PV issuer just before its product.
@@ -634,16 +635,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 uint8_t* kt = smem + OFF_RING + s * 2 * TILE_BYTES;
                 uint8_t* vt = kt + TILE_BYTES;
                 // the window holds every page's cache row.  One elected lane posts the
-                // byte count, then lanes 0-5 issue the warp's six copies at once: lane
-                // 3 jj + c copies page pg0 + jj, c = 0 / 1 the K halves, c = 2 its V
-                mbar_arrive_expect_tx_elect(bar, bytes);
+                // byte count, then lanes 0-3 issue the warp's four copies at once: lane
+                // 2 jj + c copies page pg0 + jj of K (c = 0) or V (c = 1), one box each
+                mbar_arrive_expect_tx_relaxed_elect(bar, bytes);
                 {
-                    const int jj = lane / 3, c = lane - 3 * jj;
+                    const int jj = lane >> 1, c = lane & 1;
                     const int j = pg0 + jj;
                     const int y = __shfl_sync(0xffffffffu, win_y,
                                               ((t - gr.t_lo) % WIN_TILES) * (KT / 16) + j);
-                    if (lane < 3 * (KT / 32) && j < pages) {
-                        if (c < 2) tma_load_2d(kt + c * (KT * 128) + j * 2048, &kmap, bar, c * 64, y, policy);
+                    if (lane < 2 * (KT / 32) && j < pages) {
+                        if (c == 0) tma_load_4d_hint(kt + j * 4096, &kmap, bar, 0, 0, 0, y >> 3, policy);
                         else tma_load_3d_hint(vt + j * 4096, &vmap, bar, 0, y, 0, policy);
                     }
                     __syncwarp();
@@ -695,7 +696,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t ad = smem_desc_sw128(qa + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * (KT * 128) + (kk & 3) * 32, 16, 1024);
+                    // K is [page][row group][half][8 rows][128 bytes]: the 8-key groups
+                    // of the tile are 2 KB apart, the halves 1 KB
+                    const uint64_t bd = smem_desc_sw128(ka + (kk >> 2) * 1024 + (kk & 3) * 32, 16, 2048);
                     tc_mma_bf16_elect(tS + sb * KT, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
                 tc_commit_elect(&sfull[sb]);
@@ -1351,7 +1354,7 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     if (rows >= (1LL << 31)) return TV_ERR_UNSUPPORTED;
     CUtensorMap qm, km, vm;
     if (!make_q_map(&qm, a.q, D, a.Hq, (int64_t)a.B * a.N, G, npt) ||
-        !make_cache_map(&km, a.k_cache, D, rows) || !make_page_map(&vm, a.v_cache, rows))
+        !make_kpage_map(&km, a.k_cache, rows) || !make_page_map(&vm, a.v_cache, rows))
         return TV_ERR_CUDA;
     Params prm{};
     prm.table = a.block_table;

@@ -54,6 +54,21 @@ bool make_page_map(CUtensorMap* map, const void* base, int64_t rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_kpage_map(CUtensorMap* map, const void* base, int64_t rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rows % 8 != 0) return false;
+    // (column in half, row in its group of 8, half, group of 8 rows): a box is one
+    // 16-row page laid out [group][half][8 rows][128 bytes], so the 8-row groups
+    // of consecutive pages sit 2 KB apart for either half
+    cuuint64_t dims[4] = {64, 8, 2, (cuuint64_t)(rows / 8)};
+    cuuint64_t strides[3] = {256, 128, 2048};
+    cuuint32_t box[4] = {64, 8, 2, 2};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_q_map(CUtensorMap* map, const void* base, int d, int Hq, int64_t nodes, int G,
                 int npt) {
     EncodeTiledFn enc = encode_fn();

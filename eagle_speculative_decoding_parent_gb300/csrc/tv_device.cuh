@@ -170,6 +170,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         "l"(policy)
         : "memory");
 }
+// 4-D copy with an L2 cache hint, issued by the calling thread.
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "l"(policy)
+        : "memory");
+}
 // Warp-collective forms (every lane of a converged warp calls them with the
 // same arguments): one lane chosen by elect.sync performs the operation.  The
 // warp stays converged, so the operands can stay in uniform registers; issuing
@@ -178,6 +189,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint3
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
         "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+// The same without release semantics: the bytes arrive through the copies'
+// complete_tx, so the byte count needs no ordering against the thread's
+// earlier memory accesses (a release would first wait for its outstanding
+// global loads and stores).
+__device__ __forceinline__ void mbar_arrive_expect_tx_relaxed_elect(uint64_t* bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
         "r"(bytes)
         : "memory");
 }

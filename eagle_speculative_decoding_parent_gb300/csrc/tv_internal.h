@@ -80,6 +80,7 @@ bool make_cache_map(CUtensorMap* map, const void* base, int d, int64_t rows);
 // Same cache with d = 128 viewed as 16-row pages: one box holds a page's two
 // 64-column halves, [half][16 rows][64 columns], 128-byte swizzle.
 bool make_page_map(CUtensorMap* map, const void* base, int64_t rows);
+bool make_kpage_map(CUtensorMap* map, const void* base, int64_t rows);
 // Q [B*N][Hq][d] bf16: box 64 columns x G heads x npt nodes, 128-byte swizzle.
 bool make_q_map(CUtensorMap* map, const void* base, int d, int Hq, int64_t nodes, int G,
                 int npt);
