@@ -16,9 +16,12 @@
 //   stochastic    the accept tests touch two scalars per draft (all evaluated at
 //                 once, the first failure wins); only the row(s) the emitted
 //                 token is drawn from are read, cut into chunks, one CTA per
-//                 chunk.  Integer weights make the sums exact (the draw does not
-//                 depend on summation order); the CTA that completes a sequence
-//                 picks the chunk holding the target prefix sum and searches it.
+//                 chunk, each warp streaming whole 2048-element pieces with
+//                 16-byte loads.  Integer weights make the sums exact (the draw
+//                 does not depend on summation order; they are formed as two
+//                 exact parts with packed fp32 arithmetic); the CTA that
+//                 completes a sequence picks the piece holding the target
+//                 prefix sum and searches it.
 // Cluster kernels: all CTAs of a cluster take identical control-flow decisions
 // (same inputs, same exchanged values), so every cluster barrier is reached by
 // every CTA.  Arrival counters return to zero when a call completes.
@@ -37,7 +40,6 @@ namespace {
 
 constexpr int NO_INDEX = 0x7fffffff;
 constexpr int TIMED_OUT = -2;      // a row argmax whose data did not arrive in time
-constexpr uint64_t SUM_TIMED_OUT = 1ull << 63;  // a chunk sum whose data did not arrive
 
 struct AccParams {
     const int32_t* parents;
@@ -609,12 +611,79 @@ accept_walk_kernel(AccParams p) {
     }
 }
 
+// Weights of a pair of values (x0, x1) added to the running part sums, exactly:
+// with y = min(max(x, 0), 1) (NaN -> 0) and t = y * 2^16, the weight
+// floor(y * 2^40) = H * 2^24 + L, H = floor(t) and L = floor((t - H) * 2^24) < 2^24.
+// H is taken with one round-down add of 2^23 (t <= 2^16, so the sum's unit is
+// 1); (t - H) * 2^24 is exact (one fma), and L its truncation.  H sums stay
+// exact in fp32 for up to 256 values, L sums in 32 bits for up to 256.
+__device__ __forceinline__ void weight_pair_acc(float x0, float x1, uint64_t& hacc, uint32_t& lacc) {
+    const uint64_t C23 = 0x4B0000004B000000ull;                  // (2^23, 2^23)
+    const uint64_t y = f2_pack(fminf(fmaxf(x0, 0.f), 1.f), fminf(fmaxf(x1, 0.f), 1.f));
+    const uint64_t t = f2_mul(y, 0x4780000047800000ull);        // * 2^16
+    const uint64_t h = f2_add(f2_add_rm(t, C23), 0xCB000000CB000000ull);  // floor(t)
+    const uint64_t r = f2_fma(h, 0xCB800000CB800000ull, f2_mul(t, 0x4B8000004B800000ull));  // (t - H) 2^24
+    float r0, r1;
+    f2_unpack(r, r0, r1);
+    lacc += __float2uint_rz(r0) + __float2uint_rz(r1);
+    hacc = f2_add(hacc, h);
+}
+
+// Piece sums of the weights of a (RESID: of a - b) over [lo, hi), each warp
+// taking whole pieces: eight 16-byte streaming loads per row and lane in
+// flight, exact part sums per lane (64 values each), one 64-bit shuffle
+// reduction per piece.
+template <bool RESID>
+__device__ __forceinline__ void warp_piece_sums(const float* a, const float* bq, int lo, int hi,
+                                                int np, uint64_t* psum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    const float4* b4 = reinterpret_cast<const float4*>(bq);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = warp; k < np; k += CH_WARPS) {
+        const int off = lo + k * PIECE;
+        const int n4 = min(PIECE, hi - off) >> 2;  // float4s in this piece
+        const int o4 = off >> 2;
+        uint64_t hacc = 0;  // (0.f, 0.f)
+        uint32_t lacc = 0;
+#pragma unroll 1
+        for (int r0 = 0; r0 < PIECE / 128; r0 += 8) {
+            float4 x[8], y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * (r0 + i);
+                x[i] = (e < n4) ? __ldcs(a4 + o4 + e) : z4;
+                if (RESID) y[i] = (e < n4) ? __ldcs(b4 + o4 + e) : z4;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (RESID) {
+                    weight_pair_acc(__fsub_rn(x[i].x, y[i].x), __fsub_rn(x[i].y, y[i].y), hacc, lacc);
+                    weight_pair_acc(__fsub_rn(x[i].z, y[i].z), __fsub_rn(x[i].w, y[i].w), hacc, lacc);
+                } else {
+                    weight_pair_acc(x[i].x, x[i].y, hacc, lacc);
+                    weight_pair_acc(x[i].z, x[i].w, hacc, lacc);
+                }
+            }
+        }
+        float h0, h1;
+        f2_unpack(hacc, h0, h1);
+        uint64_t w = (((uint64_t)__float2uint_rz(h0) + __float2uint_rz(h1)) << 24) + lacc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (lane == 0) psum[off / PIECE] = w;
+    }
+}
+
 // Integer weights of row a over [lo, hi) (weight(a - b) when b is given, the
-// residual; weight(a) otherwise), streamed piece by piece: the sum of every
-// PIECE-element piece k goes to psum[k] (global, thread 0 writes it).  lo is a
-// multiple of PIECE.  Every thread of the CTA calls it; false on a timeout.
+// residual; weight(a) otherwise): the sum of every PIECE-element piece k goes
+// to psum[k] (global).  lo is a multiple of PIECE.  Every thread of the CTA
+// calls it.  VEC (rows 16-byte aligned, lengths multiples of 4): each warp
+// owns whole pieces (k = warp, warp + 8, ...), every lane keeps eight 16-byte
+// streaming loads per row in flight and the warp reduces its sums with
+// shuffles, so no piece waits on a CTA barrier and no shared memory is used.
 template <bool VEC>
-__device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int hi, Ring& r,
+__device__ void piece_weight_sums(const float* a, const float* bq, int lo, int hi,
                                   uint64_t (*red)[CH_WARPS], uint64_t* psum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool resid = bq != nullptr;
@@ -635,63 +704,11 @@ __device__ bool piece_weight_sums(const float* a, const float* bq, int lo, int h
             }
             __syncthreads();
         }
-        return true;
+        return;
     }
-    const int ops = resid ? 2 : 1;
-    const uint64_t pol = l2_policy_evict_first();
-    auto issue = [&](int k) {
-        const int st = (int)((r.pc + k) % r.stg);
-        const int off = lo + k * PIECE;
-        const uint32_t bytes = (uint32_t)min(PIECE, hi - off) * 4u;
-        mbar_arrive_expect_tx(&r.full[st], bytes * ops);
-        bulk_load(r.buf + (size_t)st * ops * PIECE, a + off, bytes, &r.full[st], pol);
-        if (resid) bulk_load(r.buf + (size_t)st * ops * PIECE + PIECE, bq + off, bytes, &r.full[st], pol);
-    };
-    if (tid == 0)
-        for (int k = 0; k < min(r.stg, np); ++k) issue(k);
-    bool ok = true;
-    int k = 0;
-    for (; k < np; ++k) {
-        const uint32_t g = r.pc + k;
-        const int st = (int)(g % r.stg);
-        const bool got = mbar_wait(&r.full[st], (g / r.stg) & 1u);
-        uint64_t w = 0;
-        if (got) {
-            const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
-            const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)st * ops * PIECE);
-            const float4* y4 = x4 + PIECE / 4;
-            for (int e = tid; e < n4; e += CH_THREADS) {
-                const float4 x = x4[e];
-                if (resid) {
-                    const float4 y = y4[e];
-                    w += weight(__fsub_rn(x.x, y.x)) + weight(__fsub_rn(x.y, y.y)) +
-                         weight(__fsub_rn(x.z, y.z)) + weight(__fsub_rn(x.w, y.w));
-                } else {
-                    w += weight(x.x) + weight(x.y) + weight(x.z) + weight(x.w);
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-        if (lane == 0) red[st][warp] = w;
-        ok = __syncthreads_and(got) != 0;  // every thread is done with stage st
-        if (!ok) break;
-        if (tid == 0) {
-            uint64_t t = 0;
-            for (int q = 0; q < CH_WARPS; ++q) t += red[st][q];
-            psum[(lo + k * PIECE) / PIECE] = t;
-            if (k + r.stg < np) issue(k + r.stg);
-        }
-    }
-    if (!ok && tid == 0) {
-        // let the copies still in flight land before the shared memory is released
-        for (int j = k + 1; j < min(np, k + r.stg); ++j) {
-            const uint32_t g = r.pc + j;
-            mbar_wait(&r.full[g % r.stg], (g / r.stg) & 1u);
-        }
-    }
-    r.pc += np;
-    return ok;
+    if (resid) warp_piece_sums<true>(a, bq, lo, hi, np, psum);
+    else warp_piece_sums<false>(a, bq, lo, hi, np, psum);
+    __syncthreads();  // every piece sum of the CTA is written
 }
 
 // Picks the index holding the draw among n values v(k) from `get` (a prefix
@@ -953,7 +970,7 @@ __device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar,
 // A sequence whose tree is not a chain is walked by its chunk-0 CTA alone
 // (tree_walk_stochastic); its other CTAs return.
 template <bool VEC>
-__global__ void __launch_bounds__(CH_THREADS)
+__global__ void __launch_bounds__(CH_THREADS, 3)
 accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
                          int32_t* __restrict__ seq_tick) {
     pdl_launch_dependents();
@@ -964,12 +981,6 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     __shared__ int sflag, skstar, last, schain;
     __shared__ uint64_t red[STG][CH_WARPS];
     __shared__ uint64_t tsum[PIECE / 256];
-    extern __shared__ __align__(1024) float ring_buf[];  // [STG][2][PIECE]
-    __shared__ uint64_t full[STG];
-    if (tid == 0) {
-        for (int k = 0; k < STG; ++k) mbar_init(&full[k], 1);
-        fence_mbar_init();
-    }
     if (tid < N) {
         spar[tid] = p.parents[(int64_t)b * N + tid];
         stok[tid] = p.tokens[(int64_t)b * N + tid];
@@ -1022,12 +1033,10 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     const int np_all = (p.V + PIECE - 1) / PIECE;
     const int per = ((np_all + ch - 1) / ch) * PIECE;
     uint64_t* psum = sums + (int64_t)b * np_all;
-    Ring ring{ring_buf, full, 0u, STG};
     {
         const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
-        const bool ok = piece_weight_sums<VEC>(rowa, rowb, lo, hi, ring, red, psum);
+        piece_weight_sums<VEC>(rowa, rowb, lo, hi, red, psum);
         if (tid == 0) {
-            if (!ok) psum[lo / PIECE] = SUM_TIMED_OUT;
             __threadfence();
             last = (atomicAdd(&seq_tick[b], 1) == ch - 1);
         }
@@ -1036,35 +1045,24 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     if (!last) return;
     // this CTA completed sequence b: pick the piece holding the draw
     __threadfence();
-    __shared__ int spiece, sresid, slate;
+    __shared__ int spiece, sresid;
     __shared__ uint64_t sT;
     const uint32_t x1 = draw(p, b, rejected ? kstar : K + 1).y;
     if (warp == 0) {
-        bool late = false;
-        for (int k = lane; k < np_all; k += 32) late |= (__ldcg(psum + k) & SUM_TIMED_OUT) != 0;
-        late = __any_sync(0xffffffffu, late);
         uint64_t T = 0;
-        const int pi = late ? -1 : pick_index(np_all, x1, [&](int k) { return __ldcg(psum + k); }, T);
+        const int pi = pick_index(np_all, x1, [&](int k) { return __ldcg(psum + k); }, T);
         if (lane == 0) {
             seq_tick[b] = 0;  // leave the workspace ready for the next call
             spiece = pi;
             sT = T;
             sresid = rejected;
-            slate = late;
         }
     }
     __syncthreads();
-    if (slate) {
-        write_fail(p, b, TV_ERR_TIMEOUT);
-        return;
-    }
     if (rejected && spiece < 0) {
         // the residual has no mass: draw from the target row itself (rare: this
         // CTA sums every piece of it)
-        if (!piece_weight_sums<VEC>(rowa, nullptr, 0, p.V, ring, red, psum)) {
-            write_fail(p, b, TV_ERR_TIMEOUT);
-            return;
-        }
+        piece_weight_sums<VEC>(rowa, nullptr, 0, p.V, red, psum);
         __threadfence();
         __syncthreads();  // thread 0's piece sums are visible to warp 0
         if (warp == 0) {
@@ -1129,18 +1127,6 @@ RowsWs rows_ws(int B, int N) {
     return w;
 }
 constexpr size_t ROWS_SMEM = (size_t)STG * PIECE * 4 + 1024;       // ring, one operand
-constexpr size_t STOCH_SMEM = (size_t)STG * 2 * PIECE * 4 + 1024;  // ring, two operands
-
-bool stoch_attr() {
-    static int state = -1;
-    if (state < 0)
-        state = (cudaFuncSetAttribute(accept_stochastic_kernel<true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)STOCH_SMEM) == cudaSuccess)
-                    ? 1
-                    : 0;
-    return state == 1;
-}
 
 // Clusters of cs walk CTAs that can be resident at once (0: cannot launch).
 int walk_clusters(int cs) {
@@ -1236,13 +1222,12 @@ tv_status launch_accept(const AcceptArgs& a) {
                 : cudaLaunchKernelEx(&lc.cfg, accept_walk_kernel<false>, p);
     } else {
         static int64_t cap = -1;
-        if (!stoch_attr()) return TV_ERR_CUDA;
-        if (cap < 0) cap = resident_ctas(accept_stochastic_kernel<true>, STOCH_SMEM, sms);
+        if (cap < 0) cap = resident_ctas(accept_stochastic_kernel<true>, 0, sms);
         const int ch = chunks_for(a.B, a.V, cap);
         if ((int64_t)a.B * ch > 0x7fffffff) return TV_ERR_UNSUPPORTED;
         uint64_t* sums = reinterpret_cast<uint64_t*>(ws);
         int32_t* st = reinterpret_cast<int32_t*>(ws + stoch_ws_sums(a.B, a.V));
-        LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), vec ? STOCH_SMEM : 0, a.stream);
+        LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), 0, a.stream);
         e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<true>, p, ch, sums, st)
                 : cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<false>, p, ch, sums, st);
     }

@@ -363,6 +363,42 @@ def test_stochastic_chain_full_size_bit_exact(tv, orc):
         assert_same(got, ref)
 
 
+@pytest.mark.parametrize("V", [4096, 8196])
+def test_stochastic_chain_weight_edge_values(tv, orc, V):
+    """Chain acceptance whose residual and target rows hold every class of
+    value the fixed-point weight rule separates (infinities, NaN, values at
+    and above 1, negative zero, subnormals, values around 2^-40 where the
+    weight becomes 0 or 1, and values on 2^-16 boundaries), on rows that take
+    the streaming path (16-byte aligned, length a multiple of 4): the draw
+    must equal the oracle's bit for bit."""
+    rng = np.random.default_rng(V + 1)
+    B, N = 48, 3
+    p = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, N)).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    p[np.arange(B), 0, tok[:, 1]] = 0.0                 # the first draft is rejected
+    f = np.float32
+    sp = np.array([np.inf, np.nan, 2.0, 1.0, f(1) - f(2.0 ** -24), -0.0, 1e-40, 9.0e-13,
+                   f(2.0 ** -40), f(2.0 ** -40) * f(1.5), 3e-12, 0.5, f(2.0 ** -16),
+                   f(2.0 ** -16) + f(2.0 ** -39), -1.0, -np.inf], np.float32)
+    sq = np.array([-np.inf, np.nan, 0.0, 1e-40, -0.0, 0.25, f(2.0 ** -16)], np.float32)
+    for b in range(B):
+        free = np.setdiff1d(np.arange(V), [tok[b, 1]])
+        cols = rng.choice(free, size=sp.size + sq.size + 1, replace=False)
+        p[b, 0, cols[: sp.size]] = sp
+        q[b, 1, cols[sp.size: -1]] = sq
+        p[b, 0, cols[-1]] = q[b, 1, cols[-1]] = np.inf  # inf - inf: NaN residual
+        if b % 4 == 0:                                  # residual without mass: target row draw
+            q[b, 1, :] = np.maximum(p[b, 0, :], 0) + 1
+            q[b, 1, np.isnan(q[b, 1])] = 1.0
+    w = {"parents": np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1)), "draft_tokens": tok,
+         "p": p, "q_probs": q}
+    for seed, offset in ((3, 0), (11, 5)):
+        got = run_accept(tv, w, 1, N, seed=seed, offset=offset)
+        ref = orc.accept_stochastic(w["parents"], tok, p, q, seed, offset, N)
+        assert_same(got, ref)
+
+
 @pytest.mark.parametrize("V", [1, 5, 8, 64, 4099, 50000])
 def test_stochastic_accept_paths_small(tv, orc, V):
     """High-acceptance and degenerate draft/target pairs: all-accepted bonus
