@@ -26,6 +26,7 @@
 // (same inputs, same exchanged values), so every cluster barrier is reached by
 // every CTA.  Arrival counters return to zero when a call completes.
 #include <algorithm>
+#include <cstdlib>
 
 #include <cooperative_groups.h>
 
@@ -53,6 +54,7 @@ struct AccParams {
     int32_t* out_tokens;
     int max_path;
     int32_t* status;
+    uint64_t data_wait_ns;  // row scan: limit of a wait for streamed data (TV_WAIT_NS)
 };
 
 struct ArgBest {
@@ -204,6 +206,7 @@ struct Ring {
     uint64_t* full;    // [stg]
     uint32_t pc;       // pieces this CTA has consumed (ring position and phase)
     int stg;           // pieces in flight
+    uint64_t wait_ns;  // limit of a wait for a piece's data
 };
 
 // Calls f(x, y, i) for x = a[i..i+3] and y = b[i..i+3] (zeros without b), for
@@ -235,7 +238,7 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
         for (int k = 0; k < np; ++k) {
             const uint32_t g = r.pc + k;
             const int s = (int)(g % r.stg);
-            got = got && mbar_wait(&r.full[s], (g / r.stg) & 1u);
+            got = got && mbar_wait_for(&r.full[s], (g / r.stg) & 1u, r.wait_ns);
             if (got) {
                 const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
                 const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)s * ops * PIECE);
@@ -258,7 +261,7 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
     for (; k < np; ++k) {
         const uint32_t g = r.pc + k;
         const int s = (int)(g % r.stg);
-        const bool got = mbar_wait(&r.full[s], (g / r.stg) & 1u);
+        const bool got = mbar_wait_for(&r.full[s], (g / r.stg) & 1u, r.wait_ns);
         if (got) {
             const int off = lo + k * PIECE, n4 = min(PIECE, hi - off) >> 2;
             const float4* x4 = reinterpret_cast<const float4*>(r.buf + (size_t)s * ops * PIECE);
@@ -270,8 +273,9 @@ __device__ bool stream_rows(const float* a, const float* b, int lo, int hi, Ring
         if (tid == 0 && k + r.stg < np) issue(k + r.stg);
     }
     if (!ok && tid == 0) {
-        // let the copies still in flight land before the shared memory is released
-        for (int j = k + 1; j < min(np, k + r.stg); ++j) {
+        // let the copies still in flight (piece k and the ones issued after it)
+        // land before the shared memory is released; these waits keep the full limit
+        for (int j = k; j < min(np, k + r.stg); ++j) {
             const uint32_t g = r.pc + j;
             mbar_wait(&r.full[g % r.stg], (g / r.stg) & 1u);
         }
@@ -407,7 +411,7 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
         fence_mbar_init();
     }
     __syncthreads();
-    Ring ring{ring_buf, full, 0u, STG};
+    Ring ring{ring_buf, full, 0u, STG, p.data_wait_ns};
     const int per = chunk_len(p.V, ch);
     const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
     bool ok;
@@ -1193,6 +1197,14 @@ tv_status launch_accept(const AcceptArgs& a) {
     p.out_tokens = a.out_tokens;
     p.max_path = a.max_path;
     p.status = a.status;
+    // Test-only: TV_TEST_DATA_WAIT_NS shortens the row scan's waits for streamed
+    // data (never the waits that drain copies still in flight), so a test can
+    // make a legitimate wait run out and check the TV_ERR_TIMEOUT status.
+    p.data_wait_ns = TV_WAIT_NS;
+    if (const char* e = getenv("TV_TEST_DATA_WAIT_NS")) {
+        const unsigned long long v = strtoull(e, nullptr, 10);
+        if (v > 0 && v < TV_WAIT_NS) p.data_wait_ns = v;
+    }
     const int sms = device_sm_count();
     const bool aligned = (reinterpret_cast<uintptr_t>(a.target) & 15) == 0 &&
                          (reinterpret_cast<uintptr_t>(a.draft) & 15) == 0;

@@ -114,6 +114,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// The same wait with a caller-given limit (the acceptance row scan's data
+// waits take a shorter one from a test-only setting that exercises the timeout
+// path).  A limit shorter than TV_WAIT_NS polls without suspending, so the
+// limit is honoured even when the data is about to arrive.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (limit_ns >= TV_WAIT_NS) return mbar_wait(bar, parity);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
 // The same bounded wait for a warp that has nothing else to do for a long time
 // (microseconds): each poll lets the thread be suspended for up to 20 us until
 // the phase completes, so it takes no issue slots from the warps that share its
