@@ -20,6 +20,11 @@ Parity status of each function (the pins are in ``tests/test_oracle_*.py``):
   kv_compact        pinned (torch index_select + narrow + copy_, the operation
                     the KVCache.copy passage describes)
   tree_kv_append    pinned (closed-form rotations, plain copies, error cases)
+  ragged node counts (counts= on tree_mask, attention, accept_*, tree_kv_append)
+                    pinned (a ragged batch equals the dense functions on the
+                    batch cut to each count, sequence indices kept; junk in
+                    absent slots, absent K/V rows and blocks, and mask bits
+                    above a count change nothing)
   draft_tree        pinned (exhaustive enumeration of every token path when no
                     pruning can bite, greedy-chain and one-layer closed forms,
                     per-layer frontier / final cut recomputed with numpy and
@@ -78,20 +83,26 @@ def _c(a, dtype):
 I64 = ctypes.c_int64
 
 
-def tree_mask(parents):
-    """parents int32 [B, N] -> (mask uint64 [B, N], depth int32 [B, N], status int32 [B])."""
+def _counts(counts, B):
+    return None if counts is None else _c(counts, np.int32).reshape(B)
+
+
+def tree_mask(parents, counts=None):
+    """parents int32 [B, N] -> (mask uint64 [B, N], depth int32 [B, N], status int32 [B]).
+    counts int32 [B] (optional): node count of each tree; the rest are absent."""
     lib = _load()
     parents = _c(parents, np.int32)
     B, N = parents.shape
     mask = np.zeros((B, N), np.uint64)
     depth = np.zeros((B, N), np.int32)
     status = np.zeros(B, np.int32)
-    lib.orc_tree_mask(_p(parents), I64(B), I64(N), _p(mask), _p(depth), _p(status))
+    cnt = _counts(counts, B)
+    lib.orc_tree_mask(_p(parents), I64(B), I64(N), _p(mask), _p(depth), _p(status), _p(cnt))
     return mask, depth, status
 
 
 def attention(q, k_cache, v_cache, block_table, prefix_lens, mask, *, bf16: bool,
-              scale: float = 0.0, sel=None, nthreads: int = 1):
+              scale: float = 0.0, sel=None, nthreads: int = 1, counts=None):
     """Tree-masked paged GQA attention in double precision.
 
     q: [B, N, Hq, d]; k_cache/v_cache: [num_blocks, Hkv, bs, d]; both float32,
@@ -117,11 +128,11 @@ def attention(q, k_cache, v_cache, block_table, prefix_lens, mask, *, bf16: bool
                       _p(block_table), I64(block_table.shape[1]), _p(prefix_lens), _p(mask),
                       I64(B), I64(N), I64(Hq), I64(Hkv), I64(d), I64(bs), I64(num_blocks),
                       ctypes.c_double(scale), _p(sel_arr), I64(0 if sel is None else n),
-                      _p(out), _p(status), ctypes.c_int(nthreads))
+                      _p(out), _p(status), ctypes.c_int(nthreads), _p(_counts(counts, B)))
     return out, status
 
 
-def accept_greedy(parents, tokens, logits, max_path):
+def accept_greedy(parents, tokens, logits, max_path, counts=None):
     """Greedy acceptance -> (accept_len [B], path [B, max_path], out_tokens, status)."""
     lib = _load()
     parents = _c(parents, np.int32)
@@ -133,11 +144,12 @@ def accept_greedy(parents, tokens, logits, max_path):
     out = np.zeros((B, max_path), np.int32)
     status = np.zeros(B, np.int32)
     lib.orc_accept_greedy(_p(parents), _p(tokens), _p(logits), I64(B), I64(N), I64(V),
-                          I64(max_path), _p(acc), _p(path), _p(out), _p(status))
+                          I64(max_path), _p(acc), _p(path), _p(out), _p(status),
+                          _p(_counts(counts, B)))
     return acc, path, out, status
 
 
-def accept_stochastic(parents, tokens, p, q, seed, offset, max_path):
+def accept_stochastic(parents, tokens, p, q, seed, offset, max_path, counts=None):
     """Chain rejection sampling -> (accept_len, path, out_tokens, status)."""
     lib = _load()
     parents = _c(parents, np.int32)
@@ -151,7 +163,7 @@ def accept_stochastic(parents, tokens, p, q, seed, offset, max_path):
     status = np.zeros(B, np.int32)
     lib.orc_accept_stochastic(_p(parents), _p(tokens), _p(p), _p(q), I64(B), I64(N), I64(V),
                               ctypes.c_uint64(seed), ctypes.c_uint64(offset), I64(max_path),
-                              _p(acc), _p(path), _p(out), _p(status))
+                              _p(acc), _p(path), _p(out), _p(status), _p(_counts(counts, B)))
     return acc, path, out, status
 
 
@@ -177,7 +189,7 @@ def accept_stochastic_tree(parents, tokens, p, q, seed, offset, max_path):
 
 
 def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_lens,
-                   rope_theta=0.0):
+                   rope_theta=0.0, counts=None):
     """In-place append of the tree's K/V rows into numpy caches -> status.
 
     k_new / v_new [B][N][Hkv][d] and the caches [num_blocks][Hkv][bs][d] are
@@ -196,7 +208,7 @@ def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_le
     lib.orc_tree_kv_append(I64(elem), _p(k_new), _p(v_new), _p(dep), I64(B), I64(N), I64(Hkv),
                            I64(d), ctypes.c_double(rope_theta), _p(k_cache), _p(v_cache),
                            _p(block_table), I64(block_table.shape[1]), _p(prefix_lens), I64(bs),
-                           I64(num_blocks), _p(status))
+                           I64(num_blocks), _p(status), _p(_counts(counts, B)))
     return status
 
 

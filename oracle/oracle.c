@@ -84,18 +84,31 @@ static int orc_check_tree(const int32_t* par, int64_t N) {
     return ORC_OK;
 }
 
+/* Node count of sequence b in a batch whose trees may have fewer than N nodes
+ * ("P-EAGLE in vLLM", practice 5: shapes are kept fixed, so a sequence's tree
+ * occupies the first counts[b] of the N slots and the rest are absent);
+ * counts == NULL means every tree has N nodes.  Returns -1 for a count
+ * outside [1, N]. */
+static int64_t orc_count(const int32_t* counts, int64_t b, int64_t N) {
+    if (!counts) return N;
+    const int64_t n = counts[b];
+    return (n >= 1 && n <= N) ? n : -1;
+}
+
 /* mask[b][i] bit j set  <=>  node j is node i or an ancestor of node i.
  * depth[b][i] = number of edges from the root.  A sequence with an invalid
  * parent array gets status ORC_BAD_TREE, mask 0 and depth -1 for all its
- * nodes. */
+ * nodes; with counts, only the first counts[b] nodes exist (the others get
+ * mask 0 and depth -1) and a count outside [1, N] gives ORC_OUT_OF_RANGE. */
 int orc_tree_mask(const int32_t* parents, int64_t B, int64_t N,
-                  uint64_t* mask, int32_t* depth, int32_t* status) {
+                  uint64_t* mask, int32_t* depth, int32_t* status, const int32_t* counts) {
     for (int64_t b = 0; b < B; ++b) {
         const int32_t* par = parents + b * N;
-        int st = orc_check_tree(par, N);
+        const int64_t n = orc_count(counts, b, N);
+        int st = (n < 0) ? ORC_OUT_OF_RANGE : orc_check_tree(par, n);
         status[b] = st;
         for (int64_t i = 0; i < N; ++i) {
-            if (st != ORC_OK) {
+            if (st != ORC_OK || i >= n) {  /* absent nodes: no bits, depth -1 */
                 mask[b * N + i] = 0;
                 if (depth) depth[b * N + i] = -1;
                 continue;
@@ -140,22 +153,26 @@ static int64_t orc_slot(const int32_t* block_table, int64_t max_blocks, int64_t 
  * out is [n_sel][Hq][d] doubles.  A sequence whose prefix_len is negative,
  * whose P+N positions are not covered by valid blocks, gets status
  * ORC_OUT_OF_RANGE and zero outputs.  A node with no visible key gets zero.
+ * With counts, sequence b has counts[b] nodes: its keys are the P + counts[b]
+ * positions, only mask bits below counts[b] are read, and absent nodes get
+ * zero outputs (a count outside [1, N]: ORC_OUT_OF_RANGE).
  * The K/V cache layout is [num_blocks][Hkv][bs][d]. */
 int orc_attention(int elem, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* block_table, int64_t max_blocks,
                   const int32_t* prefix_lens, const uint64_t* mask,
                   int64_t B, int64_t N, int64_t Hq, int64_t Hkv, int64_t d, int64_t bs,
                   int64_t num_blocks, double scale, const int64_t* sel, int64_t n_sel,
-                  double* out, int32_t* status, int nthreads) {
+                  double* out, int32_t* status, int nthreads, const int32_t* counts) {
     if (Hkv <= 0 || Hq % Hkv != 0) return -1;
     int64_t G = Hq / Hkv;
     if (!(scale > 0.0)) scale = 1.0 / sqrt((double)d);
     /* per-sequence validity */
     for (int64_t b = 0; b < B; ++b) {
         int64_t P = prefix_lens[b];
+        const int64_t n = orc_count(counts, b, N);
         int st = ORC_OK;
-        if (P < 0) st = ORC_OUT_OF_RANGE;
-        for (int64_t t = 0; st == ORC_OK && t < P + N; ++t)
+        if (P < 0 || n < 0) st = ORC_OUT_OF_RANGE;
+        for (int64_t t = 0; st == ORC_OK && t < P + n; ++t)
             if (orc_slot(block_table, max_blocks, b, t, bs, num_blocks) < 0) st = ORC_OUT_OF_RANGE;
         status[b] = st;
     }
@@ -167,13 +184,14 @@ int orc_attention(int elem, const void* q, const void* k_cache, const void* v_ca
         int64_t b = flat / N, i = flat % N;
         double* o_node = out + s * Hq * d;
         memset(o_node, 0, sizeof(double) * Hq * d);
-        if (status[b] != ORC_OK) continue;
+        const int64_t n = orc_count(counts, b, N);
+        if (status[b] != ORC_OK || i >= n) continue;
         int64_t P = prefix_lens[b];
         /* visible logical positions */
         int64_t nvis = 0;
-        int64_t* vis = (int64_t*)malloc(sizeof(int64_t) * (P + N));
+        int64_t* vis = (int64_t*)malloc(sizeof(int64_t) * (P + n));
         for (int64_t t = 0; t < P; ++t) vis[nvis++] = t;
-        for (int64_t a = 0; a < N; ++a)
+        for (int64_t a = 0; a < n; ++a)
             if ((mask[b * N + i] >> a) & 1u) vis[nvis++] = P + a;
         double* sc = (double*)malloc(sizeof(double) * (nvis > 0 ? nvis : 1));
         for (int64_t h = 0; h < Hq; ++h) {
@@ -268,15 +286,16 @@ static int orc_emit(int64_t b, const int32_t* par, const int32_t* tok, int64_t c
 int orc_accept_greedy(const int32_t* parents, const int32_t* tokens, const float* logits,
                       int64_t B, int64_t N, int64_t V, int64_t max_path,
                       int32_t* accept_len, int32_t* path, int32_t* out_tokens,
-                      int32_t* status) {
+                      int32_t* status, const int32_t* counts) {
     int64_t* am = (int64_t*)malloc(sizeof(int64_t) * N);
     int* acc = (int*)malloc(sizeof(int) * N);
     int* dep = (int*)malloc(sizeof(int) * N);
     for (int64_t b = 0; b < B; ++b) {
         const int32_t* par = parents + b * N;
         const int32_t* tok = tokens + b * N;
-        int st = orc_check_tree(par, N);
-        for (int64_t c = 1; st == ORC_OK && c < N; ++c)
+        const int64_t n = orc_count(counts, b, N);  /* nodes n..N-1 are absent */
+        int st = (n < 0) ? ORC_OUT_OF_RANGE : orc_check_tree(par, n);
+        for (int64_t c = 1; st == ORC_OK && c < n; ++c)
             if (tok[c] < 0 || tok[c] >= V) st = ORC_OUT_OF_RANGE;
         if (st == ORC_OK && max_path < 1) st = ORC_OUT_OF_RANGE;
         if (st != ORC_OK) {
@@ -284,15 +303,15 @@ int orc_accept_greedy(const int32_t* parents, const int32_t* tokens, const float
             orc_accept_fail(b, max_path, accept_len, path, out_tokens);
             continue;
         }
-        for (int64_t i = 0; i < N; ++i) am[i] = orc_argmax(logits + (b * N + i) * V, V);
+        for (int64_t i = 0; i < n; ++i) am[i] = orc_argmax(logits + (b * N + i) * V, V);
         acc[0] = 1;
         dep[0] = 0;
-        for (int64_t c = 1; c < N; ++c) {
+        for (int64_t c = 1; c < n; ++c) {
             dep[c] = dep[par[c]] + 1;
             acc[c] = acc[par[c]] && ((int64_t)tok[c] == am[par[c]]);
         }
         int64_t chosen = 0;
-        for (int64_t c = 1; c < N; ++c)
+        for (int64_t c = 1; c < n; ++c)
             if (acc[c] && dep[c] > dep[chosen]) chosen = c;
         if (am[chosen] < 0) st = ORC_BAD_VALUES;
         if (st == ORC_OK)
@@ -502,23 +521,25 @@ int orc_accept_stochastic_tree(const int32_t* par, const int32_t* tok, const flo
 int orc_accept_stochastic(const int32_t* parents, const int32_t* tokens, const float* p,
                           const float* q, int64_t B, int64_t N, int64_t V, uint64_t seed,
                           uint64_t offset, int64_t max_path, int32_t* accept_len, int32_t* path,
-                          int32_t* out_tokens, int32_t* status) {
+                          int32_t* out_tokens, int32_t* status, const int32_t* counts) {
     uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * V);
     for (int64_t b = 0; b < B; ++b) {
         const int32_t* par = parents + b * N;
         const int32_t* tok = tokens + b * N;
-        int st = orc_check_tree(par, N);
+        const int64_t n = orc_count(counts, b, N);  /* nodes n..N-1 are absent */
+        int st = (n < 0) ? ORC_OUT_OF_RANGE : orc_check_tree(par, n);
         int is_chain = 1;
-        for (int64_t i = 1; i < N; ++i)
+        for (int64_t i = 1; i < n; ++i)
             if (par[i] != i - 1) is_chain = 0;
         if (st == ORC_OK && !is_chain) {
+            /* the sequence's first n rows are its whole tree */
             orc_accept_stochastic_tree(parents + b * N, tokens + b * N, p + b * N * V,
-                                       q + b * N * V, 1, N, V, seed, offset, max_path,
+                                       q + b * N * V, 1, n, V, seed, offset, max_path,
                                        accept_len + b, path + b * max_path,
                                        out_tokens + b * max_path, status + b, b);
             continue;
         }
-        for (int64_t c = 1; st == ORC_OK && c < N; ++c)
+        for (int64_t c = 1; st == ORC_OK && c < n; ++c)
             if (tok[c] < 0 || tok[c] >= V) st = ORC_OUT_OF_RANGE;
         if (st == ORC_OK && max_path < 1) st = ORC_OUT_OF_RANGE;
         if (st != ORC_OK) {
@@ -526,7 +547,7 @@ int orc_accept_stochastic(const int32_t* parents, const int32_t* tokens, const f
             orc_accept_fail(b, max_path, accept_len, path, out_tokens);
             continue;
         }
-        int64_t K = N - 1;
+        int64_t K = n - 1;
         int64_t k;
         int64_t emitted = -1;
         for (k = 1; k <= K; ++k) {
@@ -604,24 +625,26 @@ static void orc_store(int elem, void* base, int64_t idx, double x) {
  *   k'_j = k_j cos - k_{j+d/2} sin,   k'_{j+d/2} = k_{j+d/2} cos + k_j sin;
  * values (and keys when rope_theta <= 0) are copied unchanged.  A sequence
  * with P_b < 0, a depth outside [0, N) (rope only) or a position without a
- * valid block gets ORC_OUT_OF_RANGE and no write. */
+ * valid block gets ORC_OUT_OF_RANGE and no write.  With counts only the first
+ * counts[b] nodes are appended (N above reads counts[b]). */
 int orc_tree_kv_append(int64_t elem, const void* k_new, const void* v_new, const int32_t* depth,
                        int64_t B, int64_t N, int64_t Hkv, int64_t d, double rope_theta,
                        void* k_cache, void* v_cache, const int32_t* block_table,
                        int64_t max_blocks, const int32_t* prefix_lens, int64_t bs,
-                       int64_t num_blocks, int32_t* status) {
+                       int64_t num_blocks, int32_t* status, const int32_t* counts) {
     for (int64_t b = 0; b < B; ++b) {
         const int64_t P = prefix_lens[b];
+        const int64_t n = orc_count(counts, b, N);  /* only nodes < n are appended */
         int st = ORC_OK;
-        if (P < 0) st = ORC_OUT_OF_RANGE;
-        for (int64_t i = 0; st == ORC_OK && i < N; ++i) {
+        if (P < 0 || n < 0) st = ORC_OUT_OF_RANGE;
+        for (int64_t i = 0; st == ORC_OK && i < n; ++i) {
             if (orc_slot(block_table, max_blocks, b, P + i, bs, num_blocks) < 0) st = ORC_OUT_OF_RANGE;
-            if (rope_theta > 0.0 && (depth[b * N + i] < 0 || depth[b * N + i] >= N))
+            if (rope_theta > 0.0 && (depth[b * N + i] < 0 || depth[b * N + i] >= n))
                 st = ORC_OUT_OF_RANGE;
         }
         status[b] = st;
         if (st != ORC_OK) continue;
-        for (int64_t i = 0; i < N; ++i) {
+        for (int64_t i = 0; i < n; ++i) {
             const int64_t slot = orc_slot(block_table, max_blocks, b, P + i, bs, num_blocks);
             const int64_t blk = slot / bs, row = slot % bs;
             for (int64_t g = 0; g < Hkv; ++g) {
