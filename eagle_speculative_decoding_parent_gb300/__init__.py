@@ -62,19 +62,20 @@ def _sig(name, res, args):
 
 _status_string = _sig("tv_status_string", ctypes.c_char_p, [_i])
 _abi = _sig("tv_abi_version", _i, [])
-_mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p])
+_mask = _sig("tree_mask_build", _i, [_p, _i, _i, _p, _p, _p, _p, _p])
 _attn_ws = _sig("tree_verify_attention_workspace", _sz, [_i, _i, _i, _i, _i, _i, _i, _i])
 _attn_nk = _sig("tree_verify_attention_kernels", _i, [_i, _i, _i, _i, _i, _i, _i, _i, _sz])
-_append = _sig("tree_kv_append", _i, [_p, _p, _p, _i, _i, _i, _i, _f, _p, _p, _p, _i, _p, _i, _i,
-                                      _i, _p, _p])
+_append = _sig("tree_kv_append", _i, [_p, _p, _p, _i, _i, _p, _i, _i, _f, _p, _p, _p, _i, _p, _i,
+                                      _i, _i, _p, _p])
 _attn = _sig("tree_verify_attention", _i,
-             [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz, _p])
+             [_p, _p, _p, _p, _i, _p, _p, _i, _i, _p, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p, _sz,
+              _p])
 _attn_na = _sig("tree_verify_attention_noalloc", _i,
-                [_p, _p, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p])
+                [_p, _p, _p, _p, _i, _p, _p, _i, _i, _p, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p])
 _attn_na_cap = _sig("tree_verify_attention_noalloc_capacity", _sz, [])
 _acc_ws = _sig("tree_accept_workspace", _sz, [_i, _i, _i, _i])
 _acc = _sig("tree_accept", _i,
-            [_i, _p, _p, _p, _p, _i, _i, _i, _u64, _u64, _p, _p, _p, _i, _p, _p, _sz, _p])
+            [_i, _p, _p, _p, _p, _i, _i, _p, _i, _u64, _u64, _p, _p, _p, _i, _p, _p, _sz, _p])
 _compact = _sig("kv_compact", _i,
                 [_p, _p, _i, _i64, _p, _i, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p,
                  _p, _p])
@@ -83,7 +84,7 @@ _draft_ws = _sig("draft_tree_workspace", _sz, [_i, _i, _i])
 _draft_expand = _sig("draft_tree_expand", _i, [_p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p,
                                                _p, _p, _p, _sz, _p])
 
-assert _abi() == 1, "header / library ABI mismatch"
+assert _abi() == 2, "header / library ABI mismatch"
 
 
 def status_string(code: int) -> str:
@@ -118,6 +119,15 @@ def _want(t, dtype, name, shape=None):
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _counts(node_counts, B):
+    """Optional per-sequence node counts: int32 [B] on the device (the tree of
+    sequence b is its first node_counts[b] node slots); None for full trees."""
+    if node_counts is None:
+        return None
+    _want(node_counts, torch.int32, "node_counts", (B,))
+    return _ptr(node_counts)
+
+
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -131,8 +141,9 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def tree_mask_build(parents, mask, depth, status, stream=None) -> None:
-    """parents int32 [B,N] -> mask int64 (uint64 bits) [B,N], depth int32 [B,N] or None, status [B]."""
+def tree_mask_build(parents, mask, depth, status, stream=None, *, node_counts=None) -> None:
+    """parents int32 [B,N] -> mask int64 (uint64 bits) [B,N], depth int32 [B,N] or None,
+    status [B]; node_counts int32 [B] or None (trees of N nodes)."""
     _want(parents, torch.int32, "parents")
     if parents.dim() != 2:
         raise ValueError("parents is int32 [B, N]")
@@ -141,8 +152,8 @@ def tree_mask_build(parents, mask, depth, status, stream=None) -> None:
     if depth is not None:
         _want(depth, torch.int32, "depth", (B, N))
     _want(status, torch.int32, "status", (B,))
-    _check(_mask(_ptr(parents), B, N, _ptr(mask), _ptr(depth), _ptr(status), _stream(stream)),
-           "tree_mask_build")
+    _check(_mask(_ptr(parents), B, N, _counts(node_counts, B), _ptr(mask), _ptr(depth),
+                 _ptr(status), _stream(stream)), "tree_mask_build")
 
 
 def tree_verify_attention_workspace(B, N, Hq, Hkv, d, max_blocks_per_seq, block_size,
@@ -180,17 +191,19 @@ def _attention_args(q, k_cache, v_cache, block_table, prefix_lens, mask, out, st
 
 
 def tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, mask, out, status,
-                          workspace=None, *, scale: float = 0.0, stream=None) -> None:
+                          workspace=None, *, scale: float = 0.0, stream=None,
+                          node_counts=None) -> None:
     """q [B,N,Hq,d]; caches [num_blocks,Hkv,bs,d]; block_table int32 [B,max_blocks];
     prefix_lens int32 [B]; mask int64 [B,N]; out like q; status int32 [B];
-    workspace uint8 tensor (zero-filled before first use)."""
+    workspace uint8 tensor (zero-filled before first use); node_counts int32 [B]
+    or None (rows of absent nodes are not written)."""
     B, N, Hq, Hkv, d, bs, num_blocks, dt = _attention_args(q, k_cache, v_cache, block_table,
                                                            prefix_lens, mask, out, status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
-                 _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs, num_blocks, dt, scale,
-                 _ptr(out), _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)),
-           "tree_verify_attention")
+                 _ptr(prefix_lens), _ptr(mask), B, N, _counts(node_counts, B), Hq, Hkv, d, bs,
+                 num_blocks, dt, scale, _ptr(out), _ptr(status), _ptr(workspace), ws_bytes,
+                 _stream(stream)), "tree_verify_attention")
 
 
 def tree_verify_attention_noalloc_capacity() -> int:
@@ -198,7 +211,8 @@ def tree_verify_attention_noalloc_capacity() -> int:
 
 
 def tree_verify_attention_noalloc(q, k_cache, v_cache, block_table, prefix_lens, mask, out,
-                                  status, *, scale: float = 0.0, stream=None) -> None:
+                                  status, *, scale: float = 0.0, stream=None,
+                                  node_counts=None) -> None:
     """tree_verify_attention for callers that cannot hand the library a
     workspace: the scratch is a fixed array inside the library, shared by
     every call on a device (overlapping calls race on it; the C header gives
@@ -206,9 +220,9 @@ def tree_verify_attention_noalloc(q, k_cache, v_cache, block_table, prefix_lens,
     B, N, Hq, Hkv, d, bs, num_blocks, dt = _attention_args(q, k_cache, v_cache, block_table,
                                                            prefix_lens, mask, out, status)
     _check(_attn_na(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                    block_table.shape[1], _ptr(prefix_lens), _ptr(mask), B, N, Hq, Hkv, d, bs,
-                    num_blocks, dt, scale, _ptr(out), _ptr(status), _stream(stream)),
-           "tree_verify_attention_noalloc")
+                    block_table.shape[1], _ptr(prefix_lens), _ptr(mask), B, N,
+                    _counts(node_counts, B), Hq, Hkv, d, bs, num_blocks, dt, scale, _ptr(out),
+                    _ptr(status), _stream(stream)), "tree_verify_attention_noalloc")
 
 
 def tree_accept_workspace(mode, B, N, V) -> int:
@@ -216,8 +230,10 @@ def tree_accept_workspace(mode, B, N, V) -> int:
 
 
 def tree_accept(mode, parents, draft_tokens, target, draft_probs, accept_len, path, out_tokens,
-                status, *, seed: int = 0, offset: int = 0, workspace=None, stream=None) -> None:
-    """Greedy (target = logits) or stochastic chain (target = p, draft_probs = q) acceptance."""
+                status, *, seed: int = 0, offset: int = 0, workspace=None, stream=None,
+                node_counts=None) -> None:
+    """Greedy (target = logits) or stochastic (target = p, draft_probs = q) acceptance;
+    node_counts int32 [B] or None."""
     if target.dim() != 3:
         raise ValueError("target is float32 [B, N, V]")
     B, N, V = target.shape
@@ -236,14 +252,15 @@ def tree_accept(mode, parents, draft_tokens, target, draft_probs, accept_len, pa
         _want(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_acc(mode, _ptr(parents), _ptr(draft_tokens), _ptr(target), _ptr(draft_probs), B, N,
-                V, seed, offset, _ptr(accept_len), _ptr(path), _ptr(out_tokens), path.shape[1],
-                _ptr(status), _ptr(workspace), ws_bytes, _stream(stream)), "tree_accept")
+                _counts(node_counts, B), V, seed, offset, _ptr(accept_len), _ptr(path),
+                _ptr(out_tokens), path.shape[1], _ptr(status), _ptr(workspace), ws_bytes,
+                _stream(stream)), "tree_accept")
 
 
 def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_lens, status, *,
-                   rope_theta: float = 0.0, stream=None) -> None:
+                   rope_theta: float = 0.0, stream=None, node_counts=None) -> None:
     """k_new / v_new [B,N,Hkv,d]; caches [num_blocks,Hkv,bs,d]; depth int32 [B,N]
-    (needed when rope_theta > 0); status int32 [B]."""
+    (needed when rope_theta > 0); status int32 [B]; node_counts int32 [B] or None."""
     if k_new.dim() != 4 or k_cache.dim() != 4:
         raise ValueError("k_new is [B,N,Hkv,d] and the caches [num_blocks,Hkv,block_size,d]")
     B, N, Hkv, d = k_new.shape
@@ -261,7 +278,8 @@ def tree_kv_append(k_new, v_new, depth, k_cache, v_cache, block_table, prefix_le
     _want(block_table, torch.int32, "block_table")
     _want(prefix_lens, torch.int32, "prefix_lens", (B,))
     _want(status, torch.int32, "status", (B,))
-    _check(_append(_ptr(k_new), _ptr(v_new), _ptr(depth), B, N, Hkv, d, float(rope_theta),
+    _check(_append(_ptr(k_new), _ptr(v_new), _ptr(depth), B, N, _counts(node_counts, B), Hkv, d,
+                   float(rope_theta),
                    _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
                    _ptr(prefix_lens), bs, num_blocks, _dtype_code(k_cache), _ptr(status), _stream(stream)),
            "tree_kv_append")

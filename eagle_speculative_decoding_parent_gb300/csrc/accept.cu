@@ -55,7 +55,13 @@ struct AccParams {
     int max_path;
     int32_t* status;
     uint64_t data_wait_ns;  // row scan: limit of a wait for streamed data (TV_WAIT_NS)
+    const int32_t* counts;  // nullable: nodes per sequence (its tree: the first counts[b] of N)
 };
+
+// Node count of sequence b; nodes n..N-1 are absent (never checked or accepted).
+__device__ __forceinline__ int seq_count(const AccParams& p, int b) {
+    return p.counts ? p.counts[b] : p.N;
+}
 
 struct ArgBest {
     float v;
@@ -168,10 +174,12 @@ __device__ void write_path(const AccParams& p, int b, const int* spar, const int
     }
 }
 
-// Tree and token checks in the order the acceptance rule states them
-// (structure first, then token range).  One full warp; result in every lane.
-__device__ int check_inputs(const int* spar, const int* stok, int N, int V) {
+// Checks in the order the acceptance rule states them (node count in [1, Nmax],
+// then structure, then token range) over the sequence's N nodes.  One full
+// warp; result in every lane.
+__device__ int check_inputs(const int* spar, const int* stok, int N, int V, int Nmax) {
     const int lane = threadIdx.x & 31;
+    if (N < 1 || N > Nmax) return TV_ERR_OUT_OF_RANGE;
     bool tree_bad = false, tok_bad = false;
     for (int i = lane; i < N; i += 32) {
         const int pa = spar[i];
@@ -354,9 +362,8 @@ __device__ ArgBest chunk_argmax(const float* __restrict__ row, int lo, int hi, A
 // writes the result: accepted(c) = accepted(parent) and token(c) == argmax of
 // the parent's row; the deepest accepted node is emitted with its argmax.
 __device__ void walk_and_write(const AccParams& p, int b, const int* spar, const int* stok,
-                               const int* sam) {
+                               const int* sam, int N) {
     __shared__ int schosen;
-    const int N = p.N;
     if (threadIdx.x < 32) {
         // node c is accepted when every edge on its root path matches; lane takes
         // nodes lane and lane + 32: key = depth, then the lower index on ties
@@ -392,6 +399,7 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     const int N = p.N;
     const int row = blockIdx.x / ch, c = blockIdx.x % ch;
     const int b = row / N;
+    const int n = seq_count(p, b);     // rows of absent nodes are not scanned
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ ArgBest red[CH_WARPS];
     __shared__ int last;
@@ -415,7 +423,9 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     const int per = chunk_len(p.V, ch);
     const int lo = min(p.V, c * per), hi = min(p.V, lo + per);
     bool ok;
-    const ArgBest a = chunk_argmax<VEC>(p.target + (int64_t)row * p.V, lo, hi, red, ring, ok);
+    ArgBest a{-INFINITY, NO_INDEX};
+    ok = true;
+    if (row - b * N < n) a = chunk_argmax<VEC>(p.target + (int64_t)row * p.V, lo, hi, red, ring, ok);
     if (tid == 0) {
         part[(int64_t)row * CH_MAX + c] = make_int2(__float_as_int(a.v), ok ? a.i : TIMED_OUT);
         __threadfence();
@@ -463,9 +473,9 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
     }
     __syncthreads();
     if (tid < 32) {
-        int f = check_inputs(spar, stok, N, p.V);
+        int f = check_inputs(spar, stok, n, p.V, N);
         bool late = false;
-        for (int k = tid; k < N; k += 32) late |= (sam[k] == TIMED_OUT);
+        for (int k = tid; k < n && f == TV_OK; k += 32) late |= (sam[k] == TIMED_OUT);
         const bool any_late = __any_sync(0xffffffffu, late);
         if (f == TV_OK && any_late) f = TV_ERR_TIMEOUT;
         if (tid == 0) {
@@ -478,7 +488,7 @@ accept_rows_kernel(AccParams p, int ch, int2* __restrict__ part, int32_t* __rest
         write_fail(p, b, sflag);
         return;
     }
-    walk_and_write(p, b, spar, stok, sam);
+    walk_and_write(p, b, spar, stok, sam, n);
 }
 
 // Greedy acceptance, level by level: one cluster of C CTAs per sequence, CTA
@@ -496,20 +506,21 @@ accept_walk_kernel(AccParams p) {
     pdl_launch_dependents();
     pdl_wait();
     const int b = blockIdx.x / C;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, Nmax = p.N;
+    const int N = seq_count(p, b);  // the sequence's nodes; the rest are absent
     __shared__ int spar[64], stok[64], sam[64];
     __shared__ ArgBest exch[2][64];
     __shared__ ArgBest red[CH_WARPS];
     __shared__ int sflag;
     __shared__ unsigned long long snext;
-    if (tid < N) {
-        spar[tid] = p.parents[(int64_t)b * N + tid];
-        stok[tid] = p.tokens[(int64_t)b * N + tid];
+    if (tid < 64) {
+        spar[tid] = (tid < N && tid < Nmax) ? p.parents[(int64_t)b * Nmax + tid] : 0;
+        stok[tid] = (tid < N && tid < Nmax) ? p.tokens[(int64_t)b * Nmax + tid] : 0;
         sam[tid] = -1;
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V);
+        const int f = check_inputs(spar, stok, N, p.V, Nmax);
         if (tid == 0) sflag = f;
     }
     __syncthreads();
@@ -525,7 +536,7 @@ accept_walk_kernel(AccParams p) {
     for (int level = 0; level < N; ++level) {
         for (uint64_t f = frontier; f; f &= f - 1) {
             const int u = __ffsll((long long)f) - 1;
-            const float* row = p.target + ((int64_t)b * N + u) * p.V;
+            const float* row = p.target + ((int64_t)b * Nmax + u) * p.V;
             ArgBest a;
             if (VEC) {
                 a = slice_argmax_ldg(row, lo, hi, red);
@@ -841,14 +852,16 @@ __device__ int chunk_find(const float* a, const float* bq, int lo, int hi, uint6
 // row when it has no mass) with word 1 of the last rejected child's draw; a
 // leaf: the bonus token from the target row with word 1 of draw N (leaf N-1) or
 // N + leaf.  The residual is recomputed element by element from the rows.
-__device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar, const int* stok) {
-    const int N = p.N, V = p.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// N: the sequence's node count (rows keep the batch's stride p.N).
+__device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar, const int* stok,
+                                     int N) {
+    const int V = p.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ int rj[64];          // rejected children of the current node, in order
     __shared__ uint64_t rS[64];     // residual sum after each of those rejections
     __shared__ uint64_t tred[CH_WARPS];
     __shared__ int tfound;
-    const float* tgt = p.target + (int64_t)b * N * V;
-    const float* drf = p.draft + (int64_t)b * N * V;
+    const float* tgt = p.target + (int64_t)b * p.N * V;
+    const float* drf = p.draft + (int64_t)b * p.N * V;
     // weight of element t: target row (m == 0) or residual after m rejections
     auto wt = [&](const float* pc, int m, int t) -> uint64_t {
         if (m == 0) return weight(__ldg(pc + t));
@@ -980,18 +993,19 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     pdl_launch_dependents();
     pdl_wait();
     const int b = blockIdx.x / ch, c = blockIdx.x % ch;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, N = p.N;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, Nmax = p.N;
+    const int N = seq_count(p, b);  // the sequence's nodes; the rest are absent
     __shared__ int spar[64], stok[64];
     __shared__ int sflag, skstar, last, schain;
     __shared__ uint64_t red[STG][CH_WARPS];
     __shared__ uint64_t tsum[PIECE / 256];
-    if (tid < N) {
-        spar[tid] = p.parents[(int64_t)b * N + tid];
-        stok[tid] = p.tokens[(int64_t)b * N + tid];
+    if (tid < N && tid < Nmax) {
+        spar[tid] = p.parents[(int64_t)b * Nmax + tid];
+        stok[tid] = p.tokens[(int64_t)b * Nmax + tid];
     }
     __syncthreads();
     if (tid < 32) {
-        const int f = check_inputs(spar, stok, N, p.V);
+        const int f = check_inputs(spar, stok, N, p.V, Nmax);
         bool branch = false;
         for (int i = lane; i < N; i += 32) branch |= (i > 0 && spar[i] != i - 1);
         branch = __any_sync(0xffffffffu, branch);
@@ -1006,7 +1020,7 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
         return;  // every CTA of the sequence returns here: its counter is untouched
     }
     if (!schain) {
-        if (c == 0) tree_walk_stochastic(p, b, spar, stok);
+        if (c == 0) tree_walk_stochastic(p, b, spar, stok, N);
         return;  // the counter is untouched for a tree as well
     }
     // accept tests k = 1..K, all at once (counter-based draws); the first failure wins
@@ -1019,8 +1033,8 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
             if (k <= K) {
                 const uint32_t u24 = draw(p, b, k).x >> 8;
                 const int x = stok[k];
-                const float pk = __ldg(p.target + ((int64_t)b * N + (k - 1)) * p.V + x);
-                const float qk = __ldg(p.draft + ((int64_t)b * N + k) * p.V + x);
+                const float pk = __ldg(p.target + ((int64_t)b * Nmax + (k - 1)) * p.V + x);
+                const float qk = __ldg(p.draft + ((int64_t)b * Nmax + k) * p.V + x);
                 acc = __dmul_rn((double)u24, (double)qk) < __dmul_rn((double)pk, 16777216.0);
             }
             const unsigned rej = __ballot_sync(0xffffffffu, !acc);
@@ -1031,8 +1045,8 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
     __syncthreads();
     const int kstar = skstar;
     const bool rejected = kstar <= K;
-    const float* rowa = p.target + ((int64_t)b * N + (rejected ? kstar - 1 : K)) * p.V;
-    const float* rowb = rejected ? p.draft + ((int64_t)b * N + kstar) * p.V : nullptr;
+    const float* rowa = p.target + ((int64_t)b * Nmax + (rejected ? kstar - 1 : K)) * p.V;
+    const float* rowb = rejected ? p.draft + ((int64_t)b * Nmax + kstar) * p.V : nullptr;
     // chunk c: whole pieces [lo, hi); piece sums of sequence b at psum[b][*]
     const int np_all = (p.V + PIECE - 1) / PIECE;
     const int per = ((np_all + ch - 1) / ch) * PIECE;
@@ -1197,6 +1211,7 @@ tv_status launch_accept(const AcceptArgs& a) {
     p.out_tokens = a.out_tokens;
     p.max_path = a.max_path;
     p.status = a.status;
+    p.counts = a.counts;
     // Test-only: TV_TEST_DATA_WAIT_NS shortens the row scan's waits for streamed
     // data (never the waits that drain copies still in flight), so a test can
     // make a legitimate wait run out and check the TV_ERR_TIMEOUT status.

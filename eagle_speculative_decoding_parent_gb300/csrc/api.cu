@@ -50,13 +50,13 @@ const char* tv_status_string(int s) {
     }
 }
 
-int tv_abi_version(void) { return 1; }
+int tv_abi_version(void) { return 2; }
 
-tv_status tree_mask_build(const int32_t* parents, int B, int N, uint64_t* mask, int32_t* depth,
-                          int32_t* status, tv_stream_t stream) {
+tv_status tree_mask_build(const int32_t* parents, int B, int N, const int32_t* node_counts,
+                          uint64_t* mask, int32_t* depth, int32_t* status, tv_stream_t stream) {
     if (B < 0 || N < 1 || N > 64) return TV_ERR_INVALID_ARG;
     if (B > 0 && (!parents || !mask || !status)) return TV_ERR_INVALID_ARG;
-    return launch_tree_mask(parents, B, N, mask, depth, status, (cudaStream_t)stream);
+    return launch_tree_mask(parents, B, N, node_counts, mask, depth, status, (cudaStream_t)stream);
 }
 
 static bool attn_shape_ok(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs,
@@ -91,9 +91,10 @@ int tree_verify_attention_kernels(int B, int N, int Hq, int Hkv, int d, int max_
 tv_status tree_verify_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks_per_seq,
                                 const int32_t* prefix_lens, const uint64_t* mask, int B, int N,
-                                int Hq, int Hkv, int d, int block_size, int num_blocks,
-                                tv_dtype dt, float scale, void* out, int32_t* status,
-                                void* workspace, size_t workspace_bytes, tv_stream_t stream) {
+                                const int32_t* node_counts, int Hq, int Hkv, int d,
+                                int block_size, int num_blocks, tv_dtype dt, float scale,
+                                void* out, int32_t* status, void* workspace,
+                                size_t workspace_bytes, tv_stream_t stream) {
     if (dt != TV_F32 && dt != TV_BF16) return TV_ERR_INVALID_ARG;
     if (B < 0 || N < 1 || N > 64 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 ||
         block_size < 1 || num_blocks < 1)
@@ -115,6 +116,7 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
     a.max_blocks = max_blocks_per_seq;
     a.prefix_lens = prefix_lens;
     a.mask = mask;
+    a.counts = node_counts;
     a.B = B;
     a.N = N;
     a.Hq = Hq;
@@ -137,8 +139,9 @@ size_t tree_accept_workspace(tv_accept_mode mode, int B, int N, int V) {
 }
 
 tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t* draft_tokens,
-                      const float* target, const float* draft_probs, int B, int N, int V,
-                      uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* path,
+                      const float* target, const float* draft_probs, int B, int N,
+                      const int32_t* node_counts, int V, uint64_t seed, uint64_t offset,
+                      int32_t* accept_len, int32_t* path,
                       int32_t* out_tokens, int max_path, int32_t* status, void* workspace,
                       size_t workspace_bytes, tv_stream_t stream) {
     if (mode != TV_ACCEPT_GREEDY && mode != TV_ACCEPT_STOCHASTIC) return TV_ERR_INVALID_ARG;
@@ -155,6 +158,7 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
     a.tokens = draft_tokens;
     a.target = target;
     a.draft = draft_probs;
+    a.counts = node_counts;
     a.B = B;
     a.N = N;
     a.V = V;
@@ -172,7 +176,8 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
 }
 
 tv_status tree_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B, int N,
-                         int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                         const int32_t* node_counts, int Hkv, int d, float rope_theta,
+                         void* k_cache, void* v_cache,
                          const int32_t* block_table, int max_blocks_per_seq,
                          const int32_t* prefix_lens, int block_size, int num_blocks, tv_dtype dt,
                          int32_t* status, tv_stream_t stream) {
@@ -189,7 +194,7 @@ tv_status tree_kv_append(const void* k_new, const void* v_new, const int32_t* de
     if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15) ||
         (reinterpret_cast<uintptr_t>(k_cache) & 15) || (reinterpret_cast<uintptr_t>(v_cache) & 15))
         return TV_ERR_INVALID_ARG;
-    return launch_kv_append(k_new, v_new, depth, B, N, Hkv, d, rope_theta, k_cache, v_cache,
+    return launch_kv_append(k_new, v_new, depth, B, N, node_counts, Hkv, d, rope_theta, k_cache, v_cache,
                             block_table, max_blocks_per_seq, prefix_lens, block_size, num_blocks,
                             eb, status, (cudaStream_t)stream);
 }

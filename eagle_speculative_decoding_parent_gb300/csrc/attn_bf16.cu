@@ -45,6 +45,7 @@ struct Params {
     const int32_t* table;
     const int32_t* prefix_lens;
     const uint64_t* mask;
+    const int32_t* counts;  // nullable: nodes per sequence (the first counts[b] of N)
     __nv_bfloat16* out;
     int32_t* status;
     int32_t* sched;      // [0] next group, [1] CTAs finished (both return to 0)
@@ -61,14 +62,20 @@ struct Layout {
     static constexpr int XO_STRIDE = D + 4;        // floats per exchanged row (O, m, l, pad)
 };
 
-// Validity of sequence b, evaluated by one warp: prefix length in range and
-// every block id covering positions 0..P+N-1 inside the cache.
+// Nodes of sequence b (its tree is the first n of the N node slots).
+__device__ __forceinline__ int seq_nodes(const Params& p, int b) {
+    return p.counts ? p.counts[b] : p.N;
+}
+
+// Validity of sequence b, evaluated by one warp: node count in [1, N], prefix
+// length in range and every block id covering positions 0..P+n-1 inside the cache.
 __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
     const int lane = threadIdx.x & 31;
-    bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
+    const int n = seq_nodes(p, b);
+    bool ok = P >= 0 && n >= 1 && n <= p.N && (int64_t)P + n <= (int64_t)p.max_blocks * p.bs;
     if (ok) {
         // four independent loads per lane in flight per round
-        const int nb = (P + p.N + p.bs - 1) / p.bs;
+        const int nb = (P + n + p.bs - 1) / p.bs;
         const int32_t* row = p.table + (int64_t)b * p.max_blocks;
         for (int j0 = 0; j0 < nb; j0 += 128) {
             int blk[4];
@@ -85,7 +92,7 @@ __device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
 }
 
 struct Group {
-    int b, g, qt, P, L, t_lo, t_hi;  // this CTA's tiles [t_lo, t_hi)
+    int b, g, qt, P, n, L, t_lo, t_hi;  // n nodes, L = P + n keys; this CTA's tiles [t_lo, t_hi)
     bool ok;
 };
 
@@ -108,8 +115,9 @@ __device__ __forceinline__ Group decode_group(const Params& p, const int* order,
     gr.g = (gi / p.QT) % p.Hkv;
     gr.b = group_seq(p, order, gi);
     gr.P = p.prefix_lens[gr.b];
-    gr.L = gr.P + p.N;
     gr.ok = (word & GROUP_BAD) == 0;
+    gr.n = gr.ok ? seq_nodes(p, gr.b) : p.N;  // a bad sequence: every row gets zeros
+    gr.L = gr.P + gr.n;
     const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
     gr.t_lo = (int)((int64_t)T * rank / cs);
     gr.t_hi = (int)((int64_t)T * (rank + 1) / cs);
@@ -322,9 +330,10 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
 
             // rows of this thread within the packed block
             const int r0 = gr.qt * QROWS + wm * 16 + gq4, r1 = r0 + 8;
-            const bool v0 = r0 < p.M, v1 = r1 < p.M;
+            const int m_rows = gr.n * p.G;  // rows of present nodes
+            const bool v0 = r0 < m_rows, v1 = r1 < m_rows;
             const int i0 = v0 ? r0 / p.G : 0, i1 = v1 ? r1 / p.G : 0;
-            const uint64_t nmask = (p.N >= 64) ? ~0ull : ((1ull << p.N) - 1);
+            const uint64_t nmask = (gr.n >= 64) ? ~0ull : ((1ull << gr.n) - 1);
             const uint64_t mk0 = v0 ? (p.mask[(int64_t)gr.b * p.N + i0] & nmask) : 0;
             const uint64_t mk1 = v1 ? (p.mask[(int64_t)gr.b * p.N + i1] & nmask) : 0;
 
@@ -592,7 +601,7 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant
                     acc.w += w * x.w;
                 }
                 const int r = gr.qt * QROWS + lr;
-                if (r < p.M) {
+                if (r < gr.n * p.G) {
                     const float inv = inv_den[lr];
                     const int node = r / p.G, hq = gr.g * p.G + r % p.G;
                     __nv_bfloat16* dst = p.out + (((int64_t)gr.b * p.N + node) * p.Hq + hq) * D + c4;
@@ -746,6 +755,7 @@ tv_status launch_attn_bf16(const AttnArgs& a) {
     prm.table = a.block_table;
     prm.prefix_lens = a.prefix_lens;
     prm.mask = a.mask;
+    prm.counts = a.counts;
     prm.out = static_cast<__nv_bfloat16*>(a.out);
     prm.status = a.status;
     prm.sched = static_cast<int32_t*>(a.ws);

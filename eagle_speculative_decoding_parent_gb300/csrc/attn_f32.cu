@@ -2,7 +2,9 @@
 // (sequence, node, query head).  Keys are visited in groups of 32 (one per
 // lane) with an online softmax across groups; the value rows are accumulated
 // with lane-parallel output columns (coalesced).  Used for float32 caches,
-// where tensor cores would change the arithmetic.
+// where tensor cores would change the arithmetic.  With node counts, sequence
+// b's keys are its P + counts[b] positions and the rows of absent nodes are
+// not written.
 #include "tv_device.cuh"
 #include "tv_internal.h"
 
@@ -12,8 +14,9 @@ template <int DPL>  // output columns per lane (d / 32)
 __global__ void __launch_bounds__(128)
 attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
                 const float* __restrict__ vc, const int32_t* __restrict__ table, int max_blocks,
-                const int32_t* __restrict__ prefix_lens, const uint64_t* __restrict__ mask, int B,
-                int N, int Hq, int Hkv, int bs, int num_blocks, float scale,
+                const int32_t* __restrict__ prefix_lens, const uint64_t* __restrict__ mask,
+                const int32_t* __restrict__ counts, int B, int N, int Hq, int Hkv, int bs,
+                int num_blocks, float scale,
                 float* __restrict__ out, int32_t* __restrict__ status) {
     constexpr int D = DPL * 32;
     const int lane = threadIdx.x & 31;
@@ -26,8 +29,9 @@ attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
     const int i = (int)(bi % N), b = (int)(bi / N);
     const int g = h / (Hq / Hkv);
     const int P = prefix_lens[b];
-    const int64_t L = (int64_t)P + N;
-    bool ok = P >= 0 && L <= (int64_t)max_blocks * bs;
+    const int n = counts ? counts[b] : N;  // nodes n..N-1 are absent
+    const int64_t L = (int64_t)P + n;
+    bool ok = P >= 0 && n >= 1 && n <= N && L <= (int64_t)max_blocks * bs;
     if (ok) {
         const int nb = (int)((L + bs - 1) / bs);
         for (int j = lane; j < nb; j += 32) {
@@ -43,7 +47,8 @@ attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
         for (int k = 0; k < DPL; ++k) o[lane + 32 * k] = 0.f;
         return;
     }
-    const uint64_t m_tree = (N >= 64) ? mask[bi] : (mask[bi] & ((1ull << N) - 1));
+    if (i >= n) return;  // absent node: no output row
+    const uint64_t m_tree = (n >= 64) ? mask[bi] : (mask[bi] & ((1ull << n) - 1));
     const float* qr = q + gw * D;
     float acc[DPL];
 #pragma unroll
@@ -123,7 +128,8 @@ tv_status launch_attn_f32(const AttnArgs& a) {
     case DPL:                                                                                  \
         e = cudaLaunchKernelEx(&lc.cfg, attn_f32_kernel<DPL>, (const float*)a.q,              \
                                (const float*)a.k_cache, (const float*)a.v_cache, a.block_table, \
-                               a.max_blocks, a.prefix_lens, a.mask, a.B, a.N, a.Hq, a.Hkv,      \
+                               a.max_blocks, a.prefix_lens, a.mask, a.counts, a.B, a.N, a.Hq, \
+                               a.Hkv,                                                           \
                                a.bs, a.num_blocks, a.scale, (float*)a.out, a.status);           \
         break;
     switch (a.d / 32) {

@@ -53,9 +53,9 @@ extern "C" size_t tree_verify_attention_noalloc_capacity(void) { return kScratch
 
 extern "C" tv_status tree_verify_attention_noalloc(
     const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
-    int max_blocks_per_seq, const int32_t* prefix_lens, const uint64_t* mask, int B, int N, int Hq,
-    int Hkv, int d, int block_size, int num_blocks, tv_dtype dt, float scale, void* out,
-    int32_t* status, tv_stream_t stream) {
+    int max_blocks_per_seq, const int32_t* prefix_lens, const uint64_t* mask, int B, int N,
+    const int32_t* node_counts, int Hq, int Hkv, int d, int block_size, int num_blocks, tv_dtype dt,
+    float scale, void* out, int32_t* status, tv_stream_t stream) {
     if (dt != TV_F32 && dt != TV_BF16) return TV_ERR_INVALID_ARG;
     if (B < 0 || N < 1 || N > 64 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_blocks_per_seq < 1 ||
         block_size < 1 || num_blocks < 1)
@@ -78,6 +78,6 @@ extern "C" tv_status tree_verify_attention_noalloc(
     // query gives for this shape, so this call takes the same schedule as a
     // tree_verify_attention call whose caller sized its workspace by that query.
     return tree_verify_attention(q, k_cache, v_cache, block_table, max_blocks_per_seq,
-                                 prefix_lens, mask, B, N, Hq, Hkv, d, block_size, num_blocks, dt,
-                                 scale, out, status, scratch, need, stream);
+                                 prefix_lens, mask, B, N, node_counts, Hq, Hkv, d, block_size,
+                                 num_blocks, dt, scale, out, status, scratch, need, stream);
 }

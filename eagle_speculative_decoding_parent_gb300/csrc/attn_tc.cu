@@ -106,7 +106,8 @@ constexpr int MAXI = 64;                               // balanced split: pieces
 constexpr int OFF_ITEMS = OFF_GQ4 + GQ * 16;           // [MAXI] x (word, first tile, end tile, bad)
 constexpr int OFF_NITEMS = OFF_ITEMS + MAXI * 16;
 constexpr int OFF_WIN = OFF_NITEMS + 16;               // [GQ][32] first-window cache rows
-constexpr int SMEM_BYTES = OFF_WIN + GQ * 32 * 4 + 1024;  // + alignment slack
+constexpr int OFF_CNT = OFF_WIN + GQ * 32 * 4;         // node count per sequence [LPT_MAX]
+constexpr int SMEM_BYTES = OFF_CNT + LPT_MAX * 4 + 1024;  // + alignment slack
 static_assert(OFF_CUM % 8 == 0, "int64 prefix sums");
 static_assert(OFF_ITEMS % 16 == 0 && OFF_GQ4 % 16 == 0, "int4 slots");
 // Balanced split: cost of starting a piece (Q tile, pipeline fill and drain,
@@ -120,6 +121,7 @@ struct Params {
     const int32_t* table;
     const int32_t* prefix_lens;
     const uint64_t* mask;
+    const int32_t* counts;  // nullable: nodes per sequence (its tree: the first counts[b] of N)
     __nv_bfloat16* out;
     int32_t* status;
     int32_t* sched;
@@ -131,7 +133,7 @@ struct Params {
 };
 
 struct Group {
-    int b, g, qt, P, L, t_lo, t_hi;
+    int b, g, qt, P, n, L, t_lo, t_hi;  // n nodes, L = P + n keys
     bool ok;
     bool whole;            // the piece covers all of the group's key tiles
 };
@@ -141,13 +143,23 @@ struct Item {
     int word, t_lo, t_hi;
 };
 
+// Node count of sequence b (cnts: the counts staged in shared memory, or null).
+__device__ __forceinline__ int seq_nodes(const Params& p, const int* cnts, int b) {
+    return cnts ? cnts[b] : (p.counts ? p.counts[b] : p.N);
+}
+// A sequence is usable when its node count is in [1, N] and its P + n keys
+// fit the block table.
+__device__ __forceinline__ bool seq_shape_ok(const Params& p, int P, int n) {
+    return P >= 0 && n >= 1 && n <= p.N && (int64_t)P + n <= (int64_t)p.max_blocks * p.bs;
+}
+
 // Balanced split: the run space.  Group (b, g) takes c0 + T_b units, c0 for
 // the fixed cost of starting a piece and then one per key tile; cum[0..B] is
 // the exclusive prefix sum over sequences (Hkv groups each), and lens[b] the
-// prefix length.  A sequence whose prefix length is out of range counts one
-// tile, so that one CTA owns it and reports it.  Called by every thread of the
-// CTA; B <= LPT_MAX.
-__device__ __forceinline__ void split_prefix(const Params& p, int64_t* cum, int* lens) {
+// prefix length, cnts[b] the node count.  A sequence whose prefix length or
+// node count is out of range counts one tile, so that one CTA owns it and
+// reports it.  Called by every thread of the CTA; B <= LPT_MAX.
+__device__ __forceinline__ void split_prefix(const Params& p, int64_t* cum, int* lens, int* cnts) {
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int64_t v[LPT_MAX / 32];
@@ -157,9 +169,11 @@ __device__ __forceinline__ void split_prefix(const Params& p, int64_t* cum, int*
             v[u] = 0;
             if (b < p.B) {
                 const int P = p.prefix_lens[b];
+                const int n = p.counts ? p.counts[b] : p.N;
                 lens[b] = P;
-                const bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
-                v[u] = (int64_t)((ok ? (P + p.N + KT - 1) / KT : 1) + p.c0) * p.Hkv;
+                cnts[b] = n;
+                const bool ok = seq_shape_ok(p, P, n);
+                v[u] = (int64_t)((ok ? (P + n + KT - 1) / KT : 1) + p.c0) * p.Hkv;
             }
         }
         int64_t run = 0;
@@ -187,12 +201,12 @@ __device__ __forceinline__ int64_t run_owner(int64_t x, int64_t U, int64_t L) {
     return ((x + 1) * L - 1) / U;
 }
 
-__device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P) {
+__device__ __forceinline__ bool seq_ok_warp(const Params& p, int b, int P, int n) {
     const int lane = threadIdx.x & 31;
-    bool ok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
+    bool ok = seq_shape_ok(p, P, n);
     if (ok) {
         // four independent loads per lane in flight per round
-        const int nb = (P + p.N + p.bs - 1) / p.bs;
+        const int nb = (P + n + p.bs - 1) / p.bs;
         const int32_t* row = p.table + (int64_t)b * p.max_blocks;
         for (int j0 = 0; j0 < nb; j0 += 128) {
             int blk[4];
@@ -221,7 +235,8 @@ __device__ __forceinline__ int group_seq(const Params& p, const int* order, int 
 // given), kv head, row tile; this CTA's share of its key tiles.
 template <bool SPLIT>
 __device__ __forceinline__ Group decode_group(const Params& p, const int* order, const int* lens,
-                                             const int64_t* cum, const Item& it, int rank, int cs) {
+                                             const int* cnts, const int64_t* cum, const Item& it,
+                                             int rank, int cs) {
     Group gr;
     const int word = it.word;
     const int gi = word & (GROUP_BAD - 1);
@@ -229,8 +244,9 @@ __device__ __forceinline__ Group decode_group(const Params& p, const int* order,
     gr.g = (gi / p.QT) % p.Hkv;
     gr.b = group_seq(p, order, gi);
     gr.P = lens ? lens[gr.b] : p.prefix_lens[gr.b];
-    gr.L = gr.P + p.N;
     gr.ok = (word & GROUP_BAD) == 0;
+    gr.n = gr.ok ? seq_nodes(p, cnts, gr.b) : p.N;  // a bad sequence: every row gets zeros
+    gr.L = gr.P + gr.n;
     const int T = gr.ok ? (gr.L + KT - 1) / KT : 0;
     if constexpr (SPLIT) {
         // a piece of a bad sequence reads nothing: a whole one writes zeros, a
@@ -322,6 +338,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // prefix lengths in shared memory (every sequence fits the table)
     int* lens_w = reinterpret_cast<int*>(smem + OFF_LPT);
     const int* lens = (SPLIT || (p.B > 1 && p.B <= LPT_MAX)) ? lens_w : nullptr;
+    // node counts in shared memory alongside (raw: checked where used)
+    int* cnts_w = reinterpret_cast<int*>(smem + OFF_CNT);
+    const int* cnts = lens ? cnts_w : nullptr;
     // balanced split: the run's pieces listed up front
     int4* items = reinterpret_cast<int4*>(smem + OFF_ITEMS);  // word, first tile, end tile, bad
     int* n_items = reinterpret_cast<int*>(smem + OFF_NITEMS);
@@ -332,7 +351,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int64_t U = 0, L = 0, x_lo = 0, x_hi = 0;
     int qt_me = 0;
     if constexpr (SPLIT) {
-        split_prefix(p, reinterpret_cast<int64_t*>(smem + OFF_CUM), lens_w);
+        split_prefix(p, reinterpret_cast<int64_t*>(smem + OFF_CUM), lens_w, cnts_w);
         U = cum[p.B];
         L = min((int64_t)p.lanes, U);  // every run holds at least one tile
         const int64_t lane_me = blockIdx.x / p.QT;
@@ -343,6 +362,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
     } else if (p.B > 1 && p.B <= LPT_MAX) {
         lpt_order(p.prefix_lens, p.B, lens_w, lens_w + LPT_MAX);
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) cnts_w[b] = p.counts ? p.counts[b] : p.N;
+        __syncthreads();
         order = lens_w + LPT_MAX;
     }
     // balanced split: the run's pieces as (group, first tile, end tile).  A piece
@@ -432,9 +453,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             int u = 0;
             for (int i = 0; i < n; ++i) {
                 const int b = group_seq(p, nullptr, items[i].x);
-                const int P = lens[b];
-                const bool pok = P >= 0 && (int64_t)P + p.N <= (int64_t)p.max_blocks * p.bs;
-                const int nb = pok ? (P + p.N + p.bs - 1) / p.bs : 0;
+                const int P = lens[b], nn = cnts[b];
+                const bool pok = seq_shape_ok(p, P, nn);
+                const int nb = pok ? (P + nn + p.bs - 1) / p.bs : 0;
                 const int chunks = max(1, (nb + 511) / 512);
                 for (int c = 0; c < chunks; ++c, ++u) {
                     if (u % (THREADS / 32) != warp) continue;
@@ -492,11 +513,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (gi < p.groups) {
                 const int b = group_seq(p, order, gi);
                 const int P = lens ? lens[b] : p.prefix_lens[b];
-                if (!seq_ok_warp(p, b, P)) {
+                const int nn = seq_nodes(p, cnts, b);
+                if (!seq_ok_warp(p, b, P, nn)) {
                     word |= GROUP_BAD;
                 } else if (!SPLIT) {
                     // each rank's first window: page `lane` of its share of the keys
-                    const int g = (gi / p.QT) % p.Hkv, Lg = P + p.N, T = (Lg + KT - 1) / KT;
+                    const int g = (gi / p.QT) % p.Hkv, Lg = P + nn, T = (Lg + KT - 1) / KT;
                     for (uint32_t r = 0; r < cs; ++r) {
                         const int tk = ((int)((int64_t)T * r / cs) * (KT / 16) + lane) * 16;
                         int y = 0;
@@ -567,7 +589,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             if (SPLIT && kprod && rank == 0) fetch_item(k);
             const Item it = take_item(k, SPLIT ? nullptr : &y0);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
+            const Group gr = decode_group<SPLIT>(p, order, lens, cnts, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             // cluster schedule: let the fetch warp claim item k + 1 once FETCH_LEAD
             // tiles of this one are left to issue (at once for an empty one)
@@ -604,7 +626,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     const int gi = nx.x;
                     const int nb_ = group_seq(p, nullptr, gi);
                     const int tk = (nx.y * (KT / 16) + lane) * 16;
-                    pf_blk = (tk < lens[nb_] + p.N)
+                    pf_blk = (tk < lens[nb_] + cnts[nb_])
                                  ? __ldg(p.table + (int64_t)nb_ * p.max_blocks + tk / p.bs)
                                  : 0;
                     pf_k = (int)k + 1;
@@ -666,7 +688,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (uint32_t k = 0; alive; ++k) {
             const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
+            const Group gr = decode_group<SPLIT>(p, order, lens, cnts, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
             // Q tile (npt nodes x G heads x 128 columns) of this group, loaded here
@@ -716,7 +738,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (uint32_t k = 0; alive; ++k) {
             const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
+            const Group gr = decode_group<SPLIT>(p, order, lens, cnts, cum, it, rank, cs);
             const int n = gr.t_hi - gr.t_lo;
             if (n == 0) continue;
             for (int j = 0; j < n; ++j, ++gt) {
@@ -790,13 +812,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (uint32_t k = 0;; ++k) {
             const Item it = take_item(k, nullptr);
             if ((it.word & (GROUP_BAD - 1)) >= p.groups) break;
-            const Group gr = decode_group<SPLIT>(p, order, lens, cum, it, rank, cs);
+            const Group gr = decode_group<SPLIT>(p, order, lens, cnts, cum, it, rank, cs);
             if (rank == 0 && row == 0 && gr.g == 0 && gr.qt == 0)
                 p.status[gr.b] = gr.ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
             const int n = gr.t_hi - gr.t_lo;
             const int node_l = row / p.G, head = row % p.G;
             const int node = gr.qt * p.npt + node_l;
-            const bool valid = (node_l < p.npt) && (node < p.N);
+            const bool valid = (node_l < p.npt) && (node < gr.n);  // absent nodes: no output
             // the node's ancestor bits (bits at or above N are never used: the
             // visibility word is cut at the sequence end); loaded now, first
             // needed by the group's last key tile
@@ -1046,7 +1068,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 }
                 const int nl = lr / p.G, hd = lr % p.G;
                 const int nd = gr.qt * p.npt + nl;
-                if (nl < p.npt && nd < p.N) {
+                if (nl < p.npt && nd < gr.n) {
                     __nv_bfloat16* dst = p.out + (((int64_t)gr.b * p.N + nd) * p.Hq + gr.g * p.G + hd) * D + c8;
                     uint4 v;
                     v.x = pack_bf16x2(acc[0], acc[1]);
@@ -1095,11 +1117,12 @@ __global__ void __launch_bounds__(MERGE_THREADS)
 attn_split_merge_kernel(Params p) {
     __shared__ int64_t cum[LPT_MAX + 1];
     __shared__ int lens[LPT_MAX];
+    __shared__ int cnts[LPT_MAX];
     __shared__ float2 nz[128];                // per row: max, 1 / weighted sum
     __shared__ float pw[MERGE_MW][128];       // weights of the first MERGE_MW pieces
     __shared__ int pslot[MERGE_MW];
     pdl_launch_dependents();
-    split_prefix(p, cum, lens);  // from the call's inputs: overlaps the attention kernel
+    split_prefix(p, cum, lens, cnts);  // from the call's inputs: overlaps the attention kernel
     const int tid = threadIdx.x;
     const int64_t U = cum[p.B];
     const int64_t L = min((int64_t)p.lanes, U);
@@ -1184,7 +1207,9 @@ attn_split_merge_kernel(Params p) {
         lr[v] = e / (D / 8);
         c8[v] = (e % (D / 8)) * 8;
         const int nl = lr[v] / p.G;
-        ok[v] = nl < p.npt && qt * p.npt + nl < p.N;
+        // rows of present nodes (a bad sequence: every row, zeros)
+        const int nb_ = seq_shape_ok(p, lens[b], cnts[b]) ? cnts[b] : p.N;
+        ok[v] = nl < p.npt && qt * p.npt + nl < nb_;
     }
     float acc[CH][8];
 #pragma unroll
@@ -1360,6 +1385,7 @@ tv_status launch_attn_tc(const AttnArgs& a) {
     prm.table = a.block_table;
     prm.prefix_lens = a.prefix_lens;
     prm.mask = a.mask;
+    prm.counts = a.counts;
     prm.out = static_cast<__nv_bfloat16*>(a.out);
     prm.status = a.status;
     prm.sched = static_cast<int32_t*>(a.ws);

@@ -6,7 +6,9 @@
 // (j, j + d/2) with angle (P + depth) * theta^(-2j/d); every product and sum
 // is rounded separately in double (no fused multiply-add), then the result is
 // rounded to binary32 and to the cache type.  Values (and keys without
-// rotation) are copied with 16-byte vectors.
+// rotation) are copied with 16-byte vectors.  With node counts only the first
+// counts[b] nodes of a sequence exist: the others are not appended, and a
+// count outside [1, N] is TV_ERR_OUT_OF_RANGE.
 #include <cuda_bf16.h>
 
 #include "tv_device.cuh"
@@ -26,6 +28,7 @@ struct ApParams {
     uint8_t* v_cache;
     const int32_t* table;
     const int32_t* prefix_lens;
+    const int32_t* counts;  // nullable
     int32_t* status;
     int N, Hkv, d, elem, max_blocks, bs, num_blocks;
     double theta;  // <= 0: no rotation
@@ -55,17 +58,18 @@ __global__ void __launch_bounds__(AP_THREADS) kv_append_kernel(ApParams p) {
     pdl_launch_dependents();
     pdl_wait();
     const int P = p.prefix_lens[b];
-    bool ok = P >= 0;
-    for (int n = tid; ok && n < p.N; n += AP_THREADS) {
+    const int cnt = p.counts ? p.counts[b] : p.N;  // nodes cnt..N-1 are absent
+    bool ok = P >= 0 && cnt >= 1 && cnt <= p.N;
+    for (int n = tid; ok && n < cnt; n += AP_THREADS) {
         ok = ap_slot(p, b, (int64_t)P + n) >= 0;
         if (ok && p.theta > 0.0) {
             const int dp = p.depth[(int64_t)b * p.N + n];
-            ok = dp >= 0 && dp < p.N;
+            ok = dp >= 0 && dp < cnt;
         }
     }
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     if (i == 0 && tid == 0) p.status[b] = ok ? TV_OK : TV_ERR_OUT_OF_RANGE;
-    if (!ok) return;
+    if (!ok || i >= cnt) return;
     const int64_t slot = ap_slot(p, b, (int64_t)P + i);
     const int64_t blk = slot / p.bs, row = slot % p.bs;
     const int64_t row_bytes = (int64_t)p.d * p.elem;
@@ -98,7 +102,8 @@ __global__ void __launch_bounds__(AP_THREADS) kv_append_kernel(ApParams p) {
 }  // namespace
 
 tv_status launch_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B,
-                           int N, int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                           int N, const int32_t* counts, int Hkv, int d, float rope_theta,
+                           void* k_cache, void* v_cache,
                            const int32_t* block_table, int max_blocks, const int32_t* prefix_lens,
                            int bs, int num_blocks, int elem, int32_t* status, cudaStream_t stream) {
     if (B == 0) return TV_OK;
@@ -110,6 +115,7 @@ tv_status launch_kv_append(const void* k_new, const void* v_new, const int32_t* 
     p.v_cache = static_cast<uint8_t*>(v_cache);
     p.table = block_table;
     p.prefix_lens = prefix_lens;
+    p.counts = counts;
     p.status = status;
     p.N = N;
     p.Hkv = Hkv;

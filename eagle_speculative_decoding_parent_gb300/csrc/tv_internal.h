@@ -65,6 +65,7 @@ struct AttnArgs {
     int max_blocks;
     const int32_t* prefix_lens;
     const uint64_t* mask;
+    const int32_t* counts;  // nullable: nodes per sequence (first counts[b] of N)
     int B, N, Hq, Hkv, d, bs, num_blocks;
     float scale;
     void* out;
@@ -85,8 +86,8 @@ bool make_kpage_map(CUtensorMap* map, const void* base, int64_t rows);
 bool make_q_map(CUtensorMap* map, const void* base, int d, int Hq, int64_t nodes, int G,
                 int npt);
 
-tv_status launch_tree_mask(const int32_t* parents, int B, int N, uint64_t* mask, int32_t* depth,
-                           int32_t* status, cudaStream_t stream);
+tv_status launch_tree_mask(const int32_t* parents, int B, int N, const int32_t* counts,
+                           uint64_t* mask, int32_t* depth, int32_t* status, cudaStream_t stream);
 tv_status launch_attn_f32(const AttnArgs& a);
 size_t attn_bf16_workspace(int B, int N, int Hq, int Hkv, int d, int max_blocks, int bs);
 // tensor-core (tcgen05) variant for row tiles wider than 64 rows; same workspace
@@ -97,7 +98,8 @@ tv_status launch_attn_tc(const AttnArgs& a);
 size_t attn_tc_workspace(int B, int N, int Hq, int Hkv);
 size_t attn_tc_zeroed_prefix(int B, int N, int Hq, int Hkv);
 tv_status launch_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B,
-                           int N, int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                           int N, const int32_t* counts, int Hkv, int d, float rope_theta,
+                           void* k_cache, void* v_cache,
                            const int32_t* block_table, int max_blocks, const int32_t* prefix_lens,
                            int bs, int num_blocks, int elem, int32_t* status, cudaStream_t stream);
 // kernels one tensor-core attention call launches with this workspace size
@@ -113,6 +115,7 @@ struct AcceptArgs {
     const int32_t* tokens;
     const float* target;
     const float* draft;
+    const int32_t* counts;  // nullable: nodes per sequence
     int B, N, V;
     uint64_t seed, offset;
     int32_t* accept_len;

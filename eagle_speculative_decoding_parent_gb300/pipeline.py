@@ -39,18 +39,21 @@ class VerifyStep:
         aws = tree_accept_workspace(mode, B, N, V)
         self.accept_workspace = torch.zeros(max(aws, 256), dtype=torch.uint8, device=dev)
 
-    def mask_build(self, parents, stream=None):
-        tree_mask_build(parents, self.mask, self.depth, self.st_mask, stream=stream)
+    def mask_build(self, parents, stream=None, node_counts=None):
+        tree_mask_build(parents, self.mask, self.depth, self.st_mask, stream=stream,
+                        node_counts=node_counts)
 
-    def attention(self, q, k_cache, v_cache, block_table, prefix_lens, stream=None):
+    def attention(self, q, k_cache, v_cache, block_table, prefix_lens, stream=None,
+                  node_counts=None):
         tree_verify_attention(q, k_cache, v_cache, block_table, prefix_lens, self.mask, self.out,
-                              self.st_attn, self.workspace, stream=stream)
+                              self.st_attn, self.workspace, stream=stream,
+                              node_counts=node_counts)
 
     def accept(self, mode, parents, draft_tokens, target, draft_probs=None, seed=0, offset=0,
-               stream=None):
+               stream=None, node_counts=None):
         tree_accept(mode, parents, draft_tokens, target, draft_probs, self.accept_len, self.path,
                     self.out_tokens, self.st_accept, seed=seed, offset=offset,
-                    workspace=self.accept_workspace, stream=stream)
+                    workspace=self.accept_workspace, stream=stream, node_counts=node_counts)
 
     def compact(self, k_cache, v_cache, block_table, prefix_lens, stream=None):
         kv_compact(k_cache, v_cache, block_table, prefix_lens, self.path, self.accept_len,
@@ -58,10 +61,14 @@ class VerifyStep:
                    dst_slots=self.dst_slots, stream=stream)
 
     def run(self, *, parents, q, k_cache, v_cache, block_table, prefix_lens, draft_tokens, target,
-            draft_probs=None, mode=GREEDY, seed=0, offset=0, stream=None):
-        self.mask_build(parents, stream)
-        self.attention(q, k_cache, v_cache, block_table, prefix_lens, stream)
-        self.accept(mode, parents, draft_tokens, target, draft_probs, seed, offset, stream)
+            draft_probs=None, mode=GREEDY, seed=0, offset=0, stream=None, node_counts=None):
+        """node_counts (int32 [B] on the device, or None): each sequence's tree is its
+        first node_counts[b] node slots; read on the device, so a captured step serves
+        any count vector written into the same tensor."""
+        self.mask_build(parents, stream, node_counts)
+        self.attention(q, k_cache, v_cache, block_table, prefix_lens, stream, node_counts)
+        self.accept(mode, parents, draft_tokens, target, draft_probs, seed, offset, stream,
+                    node_counts)
         self.compact(k_cache, v_cache, block_table, prefix_lens, stream)
 
     def capture(self, **step_args) -> "torch.cuda.CUDAGraph":

@@ -81,6 +81,23 @@ const char* tv_status_string(int status);
 int tv_abi_version(void);
 
 /* ------------------------------------------------------------------------
+ * Node counts ("P-EAGLE in vLLM", practice 5: shapes are kept fixed so that
+ * CUDA graphs stay valid while the drafts change).  tree_mask_build,
+ * tree_verify_attention(_noalloc), tree_accept and tree_kv_append take
+ * node_counts: a device int32 [B] array, or NULL for trees of N nodes.  With
+ * it, sequence b's tree is its first node_counts[b] nodes (node_counts[b] in
+ * [1, N]; the other slots are absent and may hold anything): absent nodes get
+ * no mask bits and depth -1, no attention output row (their rows of `out` are
+ * not written) and are never attended (the keys are positions
+ * 0 .. P_b + node_counts[b] - 1), are never accepted (a chain of
+ * node_counts[b] nodes has node_counts[b] - 1 drafts, and the draw indices
+ * that the rules below write as N read node_counts[b]), and are not
+ * appended.  A count outside [1, N] gives the sequence TV_ERR_OUT_OF_RANGE
+ * with that call's error outputs.  The values are read on the device, so one
+ * captured graph serves every count vector.
+ * ------------------------------------------------------------------------ */
+
+/* ------------------------------------------------------------------------
  * tree_mask_build — "vLLM-TreeEagle", 核心组件 / 1. TreeAttentionLayer: the
  * tree attention mask is built dynamically for an arbitrary path structure.
  *
@@ -92,8 +109,8 @@ int tv_abi_version(void);
  * gets status TV_ERR_BAD_TREE, mask 0 and depth -1 for every node.
  * Host errors: B < 0, N outside [1, 64], a NULL required pointer.
  * ------------------------------------------------------------------------ */
-tv_status tree_mask_build(const int32_t* parents, int B, int N, uint64_t* mask,
-                          int32_t* depth, int32_t* status, tv_stream_t stream);
+tv_status tree_mask_build(const int32_t* parents, int B, int N, const int32_t* node_counts,
+                          uint64_t* mask, int32_t* depth, int32_t* status, tv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * tree_verify_attention — "vLLM-TreeEagle", 技术创新点 / 1. Tree Attention
@@ -142,7 +159,8 @@ int tree_verify_attention_kernels(int B, int N, int Hq, int Hkv, int d, int max_
 tv_status tree_verify_attention(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, int max_blocks_per_seq,
                                 const int32_t* prefix_lens, const uint64_t* mask, int B, int N,
-                                int Hq, int Hkv, int d, int block_size, int num_blocks,
+                                const int32_t* node_counts, int Hq, int Hkv, int d,
+                                int block_size, int num_blocks,
                                 tv_dtype dt, float scale, void* out, int32_t* status,
                                 void* workspace, size_t workspace_bytes, tv_stream_t stream);
 
@@ -211,7 +229,8 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
 size_t tree_accept_workspace(tv_accept_mode mode, int B, int N, int V);
 
 tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t* draft_tokens,
-                      const float* target, const float* draft_probs, int B, int N, int V,
+                      const float* target, const float* draft_probs, int B, int N,
+                      const int32_t* node_counts, int V,
                       uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* path,
                       int32_t* out_tokens, int max_path, int32_t* status, void* workspace,
                       size_t workspace_bytes, tv_stream_t stream);
@@ -240,7 +259,8 @@ tv_status tree_accept(tv_accept_mode mode, const int32_t* parents, const int32_t
  * rope_theta, pointers not 16-byte aligned.
  * ------------------------------------------------------------------------ */
 tv_status tree_kv_append(const void* k_new, const void* v_new, const int32_t* depth, int B, int N,
-                         int Hkv, int d, float rope_theta, void* k_cache, void* v_cache,
+                         const int32_t* node_counts, int Hkv, int d, float rope_theta,
+                         void* k_cache, void* v_cache,
                          const int32_t* block_table, int max_blocks_per_seq,
                          const int32_t* prefix_lens, int block_size, int num_blocks, tv_dtype dt,
                          int32_t* status, tv_stream_t stream);
@@ -357,7 +377,8 @@ size_t tree_verify_attention_noalloc_capacity(void);
 tv_status tree_verify_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                         const int32_t* block_table, int max_blocks_per_seq,
                                         const int32_t* prefix_lens, const uint64_t* mask, int B,
-                                        int N, int Hq, int Hkv, int d, int block_size,
+                                        int N, const int32_t* node_counts, int Hq, int Hkv, int d,
+                                        int block_size,
                                         int num_blocks, tv_dtype dt, float scale, void* out,
                                         int32_t* status, tv_stream_t stream);
 

@@ -46,32 +46,32 @@ def test_status_strings_and_version(lib):
     for code in range(9):
         assert lib.tv_status_string(code)
     assert lib.tv_status_string(99) == b"unknown status"
-    assert lib.tv_abi_version() == 1
+    assert lib.tv_abi_version() == 2
 
 
 def test_host_argument_checks_need_no_gpu(lib):
     p = ctypes.c_void_p
     # N outside [1, 64]
-    assert lib.tree_mask_build(p(0), 1, 65, p(0), p(0), p(0), p(0)) == 1
-    assert lib.tree_mask_build(p(0), -1, 4, p(0), p(0), p(0), p(0)) == 1
+    assert lib.tree_mask_build(p(0), 1, 65, None, p(0), p(0), p(0), p(0)) == 1
+    assert lib.tree_mask_build(p(0), -1, 4, None, p(0), p(0), p(0), p(0)) == 1
     # B == 0: nothing to do, no launch
-    assert lib.tree_mask_build(p(0), 0, 4, p(0), p(0), p(0), p(0)) == 0
+    assert lib.tree_mask_build(p(0), 0, 4, None, p(0), p(0), p(0), p(0)) == 0
     # stochastic acceptance needs draft probabilities
     f = lib.tree_accept
-    f.argtypes = [ctypes.c_int, p, p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+    f.argtypes = [ctypes.c_int, p, p, p, p, ctypes.c_int, ctypes.c_int, p, ctypes.c_int,
                   ctypes.c_uint64, ctypes.c_uint64, p, p, p, ctypes.c_int, p, p, ctypes.c_size_t, p]
     nz = p(16)
-    assert f(1, nz, nz, nz, None, 2, 4, 10, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1
-    assert f(0, nz, nz, nz, None, 2, 4, 0, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1  # V = 0
+    assert f(1, nz, nz, nz, None, 2, 4, None, 10, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1
+    assert f(0, nz, nz, nz, None, 2, 4, None, 0, 0, 0, nz, nz, nz, 4, nz, None, 0, None) == 1
     # attention: head size 96 is not built for bf16 -> unsupported
     a = lib.tree_verify_attention
-    a.argtypes = [p, p, p, p, ctypes.c_int, p, p] + [ctypes.c_int] * 8 + \
-        [ctypes.c_float, p, p, p, ctypes.c_size_t, p]
-    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, 8, 2, 96, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
+    a.argtypes = [p, p, p, p, ctypes.c_int, p, p, ctypes.c_int, ctypes.c_int, p] + \
+        [ctypes.c_int] * 6 + [ctypes.c_float, p, p, p, ctypes.c_size_t, p]
+    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, None, 8, 2, 96, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
              None) == 4
     # Hq not a multiple of Hkv -> invalid
-    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, 6, 4, 128, 16, 10, 1, 0.0, nz, nz, nz, 1 << 20,
-             None) == 1
+    assert a(nz, nz, nz, nz, 4, nz, nz, 1, 4, None, 6, 4, 128, 16, 10, 1, 0.0, nz, nz, nz,
+             1 << 20, None) == 1
     # kernel count query: rejected shapes -> -1, empty batch -> 0 (no device needed)
     k = lib.tree_verify_attention_kernels
     k.argtypes = [ctypes.c_int] * 8 + [ctypes.c_size_t]
@@ -80,10 +80,11 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert k(0, 4, 8, 2, 128, 10, 16, 1, 0) == 0
     # tree_kv_append: host-side argument checks (nothing is launched)
     ap = lib.tree_kv_append
-    ap.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
-                   p, p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p]
-    args = lambda B, N, Hkv, d, theta, depth, dt=1: (nz, nz, depth, B, N, Hkv, d, theta, nz, nz,
-                                                     nz, 4, nz, 16, 10, dt, nz, None)
+    ap.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, p, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_float, p, p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_int, p, p]
+    args = lambda B, N, Hkv, d, theta, depth, dt=1: (nz, nz, depth, B, N, None, Hkv, d, theta, nz,
+                                                     nz, nz, 4, nz, 16, 10, dt, nz, None)
     assert ap(*args(1, 65, 2, 128, 0.0, nz)) == 1          # more than 64 nodes
     assert ap(*args(1, 4, 2, 127, 0.0, nz)) == 1           # odd head size
     assert ap(*args(1, 4, 2, 4, 0.0, nz)) == 4             # 8-byte rows: not 16-byte vectors
