@@ -301,8 +301,11 @@ def run_ours(args):
     dtype = d["q"].dtype
     step = VerifyStep(B=B, N=N, Hq=s.Hq, Hkv=s.Hkv, d=s.d, max_blocks=w["block_table"].shape[1],
                       bs=s.bs, dtype=dtype, max_path=mp, V=s.V, mode=mode)
-    # kernels per step: mask, accept and compaction launch one each; attention one,
-    # or two when it takes the balanced schedule (a merge kernel follows)
+    # kernels per step: mask and compaction launch one each; attention one, or two
+    # when it takes the balanced schedule (a merge kernel follows); acceptance one,
+    # or two for the stochastic rule on trees of more than two nodes (chains, then
+    # branching trees)
+    accept_kernels = 2 if (mode == tv.STOCHASTIC and N > 2) else 1
     attn_kernels = tv.tree_verify_attention_kernels(
         B, N, s.Hq, s.Hkv, s.d, w["block_table"].shape[1], s.bs, dtype,
         step.workspace.numel())
@@ -453,7 +456,7 @@ def run_ours(args):
                 "cpu_baseline": cpu,
                 "e2e": {"value": whole_job_rate(world, B, N, e2e_ms), "unit": UNIT,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": (3 + attn_kernels) * args.steps,
+                "gpu_launches": (2 + accept_kernels + attn_kernels) * args.steps,
                 "clocks": clocks,
                 "kernel_ms": {n: float(m) for n, m in zip(names, mean_ms)},
                 "attention_kv_gbs": attn_gbs,

@@ -840,105 +840,223 @@ __device__ int chunk_find(const float* a, const float* bq, int lo, int hi, uint6
     return sfound;
 }
 
-// Stochastic acceptance on a branching tree, walked by one CTA for sequence b
-// (multi-candidate rejection sampling: the children of the current node are
-// tried in node order).  The first child of a node takes the chain's exact
-// test; after a rejection the target is the residual max(0, p - q) kept as
-// exact integer weights: after the first rejected child c,
-// w_t = weight(p_cur,t - q_c,t); after each further one c',
-// w_t <- max(0, w_t - floor(weight(q_c',t) * S / 2^40)) with S the sum before.
-// A later child c' is accepted iff u24 * weight(q_c'(x)) * S < w_x * 2^64.
-// All children rejected: the token is drawn from the residual (from the target
-// row when it has no mass) with word 1 of the last rejected child's draw; a
-// leaf: the bonus token from the target row with word 1 of draw N (leaf N-1) or
-// N + leaf.  The residual is recomputed element by element from the rows.
-// N: the sequence's node count (rows keep the batch's stride p.N).
-__device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar, const int* stok,
-                                     int N) {
-    const int V = p.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Stochastic acceptance on a branching tree (multi-candidate rejection
+// sampling: the children of the current node are tried in node order), one
+// cluster of C CTAs per sequence, CTA `rank` owning vocabulary slice
+// [rank * per, ...).  The first child of a node takes the chain's exact test;
+// after a rejection the target is the residual max(0, p - q) kept as exact
+// integer weights: after the first rejected child c, w_t = weight(p_cur,t -
+// q_c,t); after each further one c', w_t <- max(0, w_t - floor(weight(q_c',t)
+// * S / 2^40)) with S the sum before.  A later child c' is accepted iff u24 *
+// weight(q_c'(x)) * S < w_x * 2^64.  All children rejected: the token is drawn
+// from the residual (from the target row when it has no mass) with word 1 of
+// the last rejected child's draw; a leaf: the bonus token from the target row
+// with word 1 of draw N (leaf N-1) or N + leaf.  N: the sequence's node count
+// (rows keep the batch's stride p.N).
+//
+// The residual is recomputed entry by entry from the rows.  Every pass over the
+// vocabulary (a residual sum, the draw) is split over the cluster: each CTA
+// reduces its slice, the partial sums are exchanged through distributed shared
+// memory and added in rank order, so every CTA holds the same exact integer
+// sums, takes the same decisions and reaches every cluster barrier.  The CTA
+// whose slice holds the draw finds the token with block scans and posts it to
+// rank 0, which writes the result.  Chains and invalid inputs are left to
+// accept_stochastic_kernel, launched just before on the same stream.
+constexpr int TW_U = 8;                         // 16-byte positions per thread per tile
+constexpr int TW_TILE = TW_U * CH_THREADS * 4;  // vocabulary entries per tile
+
+template <bool VEC>
+__global__ void __launch_bounds__(CH_THREADS)
+accept_stochastic_tree_kernel(AccParams p) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    pdl_launch_dependents();
+    pdl_wait();
+    const int b = blockIdx.x / C;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, Nmax = p.N, V = p.V;
+    const int N = seq_count(p, b);
+    __shared__ int spar[64], stok[64];
+    __shared__ int sflag, schain, sfound, xtok;
     __shared__ int rj[64];          // rejected children of the current node, in order
     __shared__ uint64_t rS[64];     // residual sum after each of those rejections
     __shared__ uint64_t tred[CH_WARPS];
-    __shared__ int tfound;
-    const float* tgt = p.target + (int64_t)b * p.N * V;
-    const float* drf = p.draft + (int64_t)b * p.N * V;
-    // weight of element t: target row (m == 0) or residual after m rejections
+    __shared__ uint64_t xpart[2];   // this slice's sum, by pass parity (read by the cluster)
+    if (tid < 64) {
+        spar[tid] = (tid < N && tid < Nmax) ? p.parents[(int64_t)b * Nmax + tid] : 0;
+        stok[tid] = (tid < N && tid < Nmax) ? p.tokens[(int64_t)b * Nmax + tid] : 0;
+    }
+    if (tid == 0) xtok = -1;
+    __syncthreads();
+    if (tid < 32) {
+        const int f = check_inputs(spar, stok, N, V, Nmax);
+        bool branch = false;
+        if (f == TV_OK)
+            for (int i = lane; i < N; i += 32) branch |= (i > 0 && spar[i] != i - 1);
+        branch = __any_sync(0xffffffffu, branch);
+        if (tid == 0) {
+            sflag = f;
+            schain = !branch;
+        }
+    }
+    __syncthreads();
+    // uniform across the cluster, before its first barrier
+    if (sflag != TV_OK || schain) return;
+
+    const int per = chunk_len(V, C);
+    const int lo = min(V, rank * per), hi = min(V, lo + per);
+    const float* tgt = p.target + (int64_t)b * Nmax * V;
+    const float* drf = p.draft + (int64_t)b * Nmax * V;
+    auto sub_floor = [](uint64_t w, uint64_t qw, uint64_t S) -> uint64_t {
+        const uint64_t d = (__umul64hi(qw, S) << 24) | ((qw * S) >> 40);  // floor(qw * S / 2^40)
+        return w > d ? w - d : 0ull;
+    };
+    // weight of entry t: the target row pc (m == 0) or the residual after m rejections
     auto wt = [&](const float* pc, int m, int t) -> uint64_t {
         if (m == 0) return weight(__ldg(pc + t));
         uint64_t w = weight(__fsub_rn(__ldg(pc + t), __ldg(drf + (int64_t)rj[0] * V + t)));
-        for (int j = 1; j < m; ++j) {
-            const uint64_t qw = weight(__ldg(drf + (int64_t)rj[j] * V + t));
-            const uint64_t S = rS[j - 1];
-            const uint64_t d = (__umul64hi(qw, S) << 24) | ((qw * S) >> 40);  // floor(qw * S / 2^40)
-            w = w > d ? w - d : 0ull;
-        }
+        for (int j = 1; j < m; ++j)
+            w = sub_floor(w, weight(__ldg(drf + (int64_t)rj[j] * V + t)), rS[j - 1]);
         return w;
     };
-    auto block_sum = [&](const float* pc, int m) -> uint64_t {
-        uint64_t sacc = 0;
-        for (int t = tid; t < V; t += CH_THREADS) sacc += wt(pc, m, t);
+    // this thread's entries of the tile at `base`: position u holds entries
+    // base + (u * CH_THREADS + tid) * 4 + 0..3, read as 0 outside [lo, hi); one
+    // row's loads are all issued before any is used
+    auto load_tile = [&](const float* row, int base, float (&a)[TW_U][4]) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
-        __syncthreads();
-        if (lane == 0) tred[warp] = sacc;
-        __syncthreads();
-        uint64_t tot = 0;
+        for (int u = 0; u < TW_U; ++u) {
+            const int t = base + (u * CH_THREADS + tid) * 4;
+            if (VEC) {  // hi is a multiple of 4 here
+                const float4 v = (t < hi) ? __ldg(reinterpret_cast<const float4*>(row + t))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                a[u][0] = v.x;
+                a[u][1] = v.y;
+                a[u][2] = v.z;
+                a[u][3] = v.w;
+            } else {
 #pragma unroll
-        for (int i = 0; i < CH_WARPS; ++i) tot += tred[i];
+                for (int c = 0; c < 4; ++c) a[u][c] = (t + c < hi) ? __ldg(row + t + c) : 0.f;
+            }
+        }
+    };
+    auto tile_weights = [&](const float* pc, int m, int base, uint64_t (&w)[TW_U][4]) {
+        float a[TW_U][4];
+        load_tile(pc, base, a);
+        if (m == 0) {
+#pragma unroll
+            for (int u = 0; u < TW_U; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) w[u][c] = weight(a[u][c]);
+            return;
+        }
+        float q[TW_U][4];
+        load_tile(drf + (int64_t)rj[0] * V, base, q);
+#pragma unroll
+        for (int u = 0; u < TW_U; ++u)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) w[u][c] = weight(__fsub_rn(a[u][c], q[u][c]));
+        for (int j = 1; j < m; ++j) {
+            load_tile(drf + (int64_t)rj[j] * V, base, q);
+            const uint64_t S = rS[j - 1];
+#pragma unroll
+            for (int u = 0; u < TW_U; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) w[u][c] = sub_floor(w[u][c], weight(q[u][c]), S);
+        }
+    };
+    // the sum over the vocabulary of the weights (pc, m); `before`: the sum over
+    // the slices of lower ranks, `mine`: over this slice
+    int par = 0;
+    auto cluster_sum = [&](const float* pc, int m, uint64_t& before, uint64_t& mine) -> uint64_t {
+        uint64_t acc = 0;
+        for (int base = lo; base < hi; base += TW_TILE) {
+            uint64_t w[TW_U][4];
+            tile_weights(pc, m, base, w);
+#pragma unroll
+            for (int u = 0; u < TW_U; ++u) acc += (w[u][0] + w[u][1]) + (w[u][2] + w[u][3]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) tred[warp] = acc;
+        __syncthreads();
+        uint64_t own = 0;
+#pragma unroll
+        for (int i = 0; i < CH_WARPS; ++i) own += tred[i];
+        if (tid == 0) xpart[par] = own;
+        cluster.sync();  // also orders every thread's reads of tred before its next writes
+        const uint64_t x = (lane < C) ? *cluster.map_shared_rank(&xpart[par], lane) : 0ull;
+        uint64_t tot = x, bef = (lane < rank) ? x : 0ull;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            tot += __shfl_xor_sync(0xffffffffu, tot, o);
+            bef += __shfl_xor_sync(0xffffffffu, bef, o);
+        }
+        par ^= 1;  // the slot read here is rewritten only after the next barrier
+        before = bef;
+        mine = own;
         return tot;
     };
-    // smallest t whose inclusive prefix sum exceeds T = floor(x * S / 2^32); -1 if S == 0
-    auto sample = [&](const float* pc, int m, uint64_t S, uint32_t x) -> int {
-        if (S == 0) return -1;
+    // the draw from weights (pc, m) with sum S > 0: the smallest t whose
+    // inclusive prefix sum exceeds T = floor(x * S / 2^32), returned to rank 0
+    auto sample = [&](const float* pc, int m, uint64_t S, uint64_t before, uint64_t mine,
+                      uint32_t x) -> int {
         const uint64_t T = (uint64_t)x * (S >> 32) + (((uint64_t)x * (S & 0xffffffffull)) >> 32);
-        if (tid == 0) tfound = -1;
-        uint64_t run = 0;
-        for (int base = 0; base < V; base += CH_THREADS * 8) {
-            uint64_t e[8], sacc = 0;
+        if (before <= T && T - before < mine) {  // this slice holds it (one CTA does)
+            if (tid == 0) sfound = -1;
+            uint64_t run = before;
+            for (int base = lo; base < hi; base += TW_TILE) {
+                uint64_t w[TW_U][4];
+                tile_weights(pc, m, base, w);
+                bool done = false;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int t = base + tid * 8 + k;
-                e[k] = (t < V) ? wt(pc, m, t) : 0ull;
-                sacc += e[k];
-            }
-            uint64_t incl = sacc;  // inclusive scan over the warp's lanes
+                for (int u = 0; u < TW_U; ++u) {
+                    const uint64_t s4 = (w[u][0] + w[u][1]) + (w[u][2] + w[u][3]);
+                    uint64_t incl = s4;  // inclusive scan over the warp's lanes
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            __syncthreads();
-            if (lane == 31) tred[warp] = incl;
-            __syncthreads();
-            uint64_t wpre = 0, total = 0;
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    __syncthreads();  // earlier readers of tred are done
+                    if (lane == 31) tred[warp] = incl;
+                    __syncthreads();
+                    uint64_t wpre = 0, tot = 0;
 #pragma unroll
-            for (int i = 0; i < CH_WARPS; ++i) {
-                wpre += (i < warp) ? tred[i] : 0ull;
-                total += tred[i];
-            }
-            const uint64_t excl = run + wpre + (incl - sacc);
-            if (excl <= T && T < excl + sacc) {
-                uint64_t r = excl;
+                    for (int i = 0; i < CH_WARPS; ++i) {
+                        wpre += (i < warp) ? tred[i] : 0ull;
+                        tot += tred[i];
+                    }
+                    const uint64_t ex = run + wpre + (incl - s4);
+                    if (ex <= T && T - ex < s4) {  // this thread's four entries hold it
+                        uint64_t r = ex;
+                        int hit = -1;  // the first entry whose inclusive prefix exceeds T
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    r += e[k];
-                    if (r > T) {
-                        tfound = base + tid * 8 + k;
+                        for (int c = 0; c < 4; ++c) {
+                            r += w[u][c];
+                            if (hit < 0 && r > T) hit = c;
+                        }
+                        sfound = base + (u * CH_THREADS + tid) * 4 + hit;
+                    }
+                    run += tot;
+                    __syncthreads();
+                    if (sfound >= 0) {
+                        done = true;
                         break;
                     }
                 }
+                if (done) break;
             }
-            if (run + total > T) break;
-            run += total;
+            if (tid == 0) *cluster.map_shared_rank(&xtok, 0) = sfound;
         }
-        __syncthreads();
-        return tfound;
+        cluster.sync();
+        return xtok;
     };
+
     int cur = 0, token = -1;
     for (;;) {
         const float* pc = tgt + (int64_t)cur * V;
         int m = 0, next = -1, last_rej = -1;
-        uint64_t S = 0;
+        uint64_t S = 0, before = 0, mine = 0;
         for (int c = cur + 1; c < N; ++c) {
             if (spar[c] != cur) continue;
             const uint32_t u24 = draw(p, b, c).x >> 8;
@@ -958,7 +1076,7 @@ __device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar,
             __syncthreads();  // earlier readers of rj / rS are done
             if (tid == 0) rj[m] = c;
             __syncthreads();
-            S = block_sum(pc, m + 1);
+            S = cluster_sum(pc, m + 1, before, mine);
             if (tid == 0) rS[m] = S;
             __syncthreads();
             ++m;
@@ -969,23 +1087,27 @@ __device__ void tree_walk_stochastic(const AccParams& p, int b, const int* spar,
             cur = next;
             continue;
         }
-        if (last_rej < 0) {  // a leaf: bonus token from the target row
-            const uint32_t x1 = draw(p, b, (cur == N - 1) ? N : N + cur).y;
-            token = sample(pc, 0, block_sum(pc, 0), x1);
-        } else {
-            const uint32_t x1 = draw(p, b, last_rej).y;
-            token = (S > 0) ? sample(pc, m, S, x1) : sample(pc, 0, block_sum(pc, 0), x1);
+        // a leaf: the bonus token from the target row; all children rejected: from
+        // the residual, or from the target row when the residual has no mass
+        const uint32_t x1 = (last_rej < 0) ? draw(p, b, (cur == N - 1) ? N : N + cur).y
+                                           : draw(p, b, last_rej).y;
+        if (last_rej < 0 || S == 0) {
+            m = 0;
+            S = cluster_sum(pc, 0, before, mine);
         }
+        token = (S > 0) ? sample(pc, m, S, before, mine, x1) : -1;
         break;
     }
-    if (token < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
-    else write_path(p, b, spar, stok, cur, token);
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    if (rank == 0) {
+        if (token < 0) write_fail(p, b, TV_ERR_BAD_VALUES);
+        else write_path(p, b, spar, stok, cur, token);
+    }
 }
 
 // Stochastic chain acceptance: CTA (b, c) takes chunk c of the row the token
 // is drawn from; ws: sums[b][ceil(V / PIECE)] (weight sum of every piece), seq_tick[b].
-// A sequence whose tree is not a chain is walked by its chunk-0 CTA alone
-// (tree_walk_stochastic); its other CTAs return.
+// A sequence whose tree is not a chain is left to accept_stochastic_tree_kernel.
 template <bool VEC>
 __global__ void __launch_bounds__(CH_THREADS, 3)
 accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
@@ -1019,10 +1141,7 @@ accept_stochastic_kernel(AccParams p, int ch, uint64_t* __restrict__ sums,
         if (c == 0) write_fail(p, b, sflag);
         return;  // every CTA of the sequence returns here: its counter is untouched
     }
-    if (!schain) {
-        if (c == 0) tree_walk_stochastic(p, b, spar, stok, N);
-        return;  // the counter is untouched for a tree as well
-    }
+    if (!schain) return;  // the tree kernel walks it; the counter is untouched
     // accept tests k = 1..K, all at once (counter-based draws); the first failure wins
     const int K = N - 1;
     if (warp == 0) {
@@ -1146,23 +1265,24 @@ RowsWs rows_ws(int B, int N) {
 }
 constexpr size_t ROWS_SMEM = (size_t)STG * PIECE * 4 + 1024;       // ring, one operand
 
-// Clusters of cs walk CTAs that can be resident at once (0: cannot launch).
-int walk_clusters(int cs) {
-    static int cache[17] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+using AccKernel = void (*)(AccParams);
+
+// Clusters of cs CTAs of a cluster kernel (given by its two instantiations)
+// that can be resident at once (0: cannot launch); cache[cs] keeps the answer.
+int resident_clusters(AccKernel kv, AccKernel ks, int cs, int* cache) {
     if (cs < 1 || cs > 16) return 0;
     if (cache[cs] >= 0) return cache[cs];
     int n = 0;
     bool ok = true;
     if (cs > 8)
-        ok = cudaFuncSetAttribute(accept_walk_kernel<true>,
-                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-             cudaFuncSetAttribute(accept_walk_kernel<false>,
-                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        ok = cudaFuncSetAttribute(kv, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                 cudaSuccess &&
+             cudaFuncSetAttribute(ks, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                 cudaSuccess;
     if (ok) {
         LaunchCfg lc(dim3(cs), dim3(CH_THREADS), 0, nullptr, (unsigned)cs);
         lc.cfg.numAttrs = 1;  // the cluster shape only
-        if (cudaOccupancyMaxActiveClusters(&n, accept_walk_kernel<true>, &lc.cfg) != cudaSuccess)
-            n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kv, &lc.cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     cache[cs] = n;
@@ -1171,16 +1291,27 @@ int walk_clusters(int cs) {
 
 // Largest cluster (at most 16 CTAs, at least PIECE vocabulary entries per CTA)
 // whose B clusters are resident at once; else the largest that launches.
-int walk_cluster_size(int B, int V) {
+int cluster_size_for(AccKernel kv, AccKernel ks, int* cache, int B, int V) {
     int fallback = 0;
     for (int cs = 16; cs >= 1; cs >>= 1) {
         if (cs > 1 && (int64_t)V < (int64_t)cs * PIECE) continue;
-        const int n = walk_clusters(cs);
+        const int n = resident_clusters(kv, ks, cs, cache);
         if (n <= 0) continue;
         if (n >= B) return cs;
         if (fallback == 0) fallback = cs;
     }
     return fallback;
+}
+
+int walk_cluster_size(int B, int V) {
+    static int cache[17] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    return cluster_size_for(accept_walk_kernel<true>, accept_walk_kernel<false>, cache, B, V);
+}
+
+int tree_cluster_size(int B, int V) {
+    static int cache[17] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+    return cluster_size_for(accept_stochastic_tree_kernel<true>,
+                            accept_stochastic_tree_kernel<false>, cache, B, V);
 }
 
 size_t stoch_ws_sums(int B, int V) { return align256((size_t)B * ((V + PIECE - 1) / PIECE) * 8); }
@@ -1257,6 +1388,16 @@ tv_status launch_accept(const AcceptArgs& a) {
         LaunchCfg lc(dim3((unsigned)(a.B * ch)), dim3(CH_THREADS), 0, a.stream);
         e = vec ? cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<true>, p, ch, sums, st)
                 : cudaLaunchKernelEx(&lc.cfg, accept_stochastic_kernel<false>, p, ch, sums, st);
+        // branching trees: one cluster per sequence, after the chains (every tree
+        // of at most two nodes is a chain)
+        if (e == cudaSuccess && a.N > 2) {
+            const int C = tree_cluster_size(a.B, a.V);
+            if (C <= 0) return TV_ERR_CUDA;
+            if ((int64_t)a.B * C > 0x7fffffff) return TV_ERR_UNSUPPORTED;
+            LaunchCfg lt(dim3((unsigned)(a.B * C)), dim3(CH_THREADS), 0, a.stream, (unsigned)C);
+            e = vec ? cudaLaunchKernelEx(&lt.cfg, accept_stochastic_tree_kernel<true>, p)
+                    : cudaLaunchKernelEx(&lt.cfg, accept_stochastic_tree_kernel<false>, p);
+        }
     }
     return e == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
