@@ -5,7 +5,8 @@
 // so a bad sequence is left untouched by all of them.  Keys: rotate-half pairs
 // (j, j + d/2) with angle (P + depth) * theta^(-2j/d); every product and sum
 // is rounded separately in double (no fused multiply-add), then the result is
-// rounded to binary32 and to the cache type.  Values (and keys without
+// rounded to binary32 and to the cache type; a node's (cos, sin) pairs are
+// computed once and shared by its kv heads.  Values (and keys without
 // rotation) are copied with 16-byte vectors.  With node counts only the first
 // counts[b] nodes of a sequence exist: the others are not appended, and a
 // count outside [1, N] is TV_ERR_OUT_OF_RANGE.
@@ -32,7 +33,10 @@ struct ApParams {
     int32_t* status;
     int N, Hkv, d, elem, max_blocks, bs, num_blocks;
     double theta;  // <= 0: no rotation
+    bool table_cs;  // the node's (cos, sin) table is in dynamic shared memory
 };
+
+constexpr int AP_TABLE_MAX = 3072;  // pairs per table: 48 KB of shared memory
 
 __device__ __forceinline__ int64_t ap_slot(const ApParams& p, int b, int64_t t) {
     if (t < 0) return -1;
@@ -86,13 +90,32 @@ __global__ void __launch_bounds__(AP_THREADS) kv_append_kernel(ApParams p) {
     if (p.theta <= 0.0) return;
     const int h = p.d / 2;
     const double pos = (double)(P + p.depth[(int64_t)b * p.N + i]);
+    // the angle depends on the pair, not on the kv head: each (cos, sin) is
+    // computed once per node into shared memory when the table fits
+    extern __shared__ double2 cs_tab[];  // [h] (cos, sin)
+    auto angle = [&](int j, double& sn, double& cs) {
+        sincos(__dmul_rn(pos, pow(p.theta, -2.0 * (double)j / (double)p.d)), &sn, &cs);
+    };
+    if (p.table_cs) {
+        for (int j = tid; j < h; j += AP_THREADS) {
+            double sn, cs;
+            angle(j, sn, cs);
+            cs_tab[j] = make_double2(cs, sn);
+        }
+        __syncthreads();
+    }
     for (int e = tid; e < p.Hkv * h; e += AP_THREADS) {
         const int g = e / h, j = e % h;
         const int64_t src = (((int64_t)b * p.N + i) * p.Hkv + g) * p.d;
         const int64_t dst = ((blk * p.Hkv + g) * p.bs + row) * p.d;
-        const double ang = __dmul_rn(pos, pow(p.theta, -2.0 * (double)j / (double)p.d));
         double sn, cs;
-        sincos(ang, &sn, &cs);
+        if (p.table_cs) {
+            const double2 t = cs_tab[j];
+            cs = t.x;
+            sn = t.y;
+        } else {
+            angle(j, sn, cs);
+        }
         const double x1 = ap_load(p, p.k_new, src + j), x2 = ap_load(p, p.k_new, src + j + h);
         ap_store(p, p.k_cache, dst + j, __dsub_rn(__dmul_rn(x1, cs), __dmul_rn(x2, sn)));
         ap_store(p, p.k_cache, dst + j + h, __dadd_rn(__dmul_rn(x2, cs), __dmul_rn(x1, sn)));
@@ -125,7 +148,9 @@ tv_status launch_kv_append(const void* k_new, const void* v_new, const int32_t* 
     p.bs = bs;
     p.num_blocks = num_blocks;
     p.theta = (rope_theta > 0.f) ? (double)rope_theta : 0.0;
-    LaunchCfg lc(dim3((unsigned)N, (unsigned)B), dim3(AP_THREADS), 0, stream);
+    p.table_cs = p.theta > 0.0 && d / 2 <= AP_TABLE_MAX;
+    const size_t smem = p.table_cs ? (size_t)(d / 2) * sizeof(double2) : 0;
+    LaunchCfg lc(dim3((unsigned)N, (unsigned)B), dim3(AP_THREADS), smem, stream);
     return cudaLaunchKernelEx(&lc.cfg, kv_append_kernel, p) == cudaSuccess ? TV_OK : TV_ERR_CUDA;
 }
 
