@@ -64,34 +64,41 @@ __device__ __forceinline__ uint64_t dt_word(float v, int id) {
 }
 __device__ __forceinline__ int dt_word_id(uint64_t w) { return (int)~(uint32_t)w; }
 
-// Inserts x into the descending list l (distinct words; 0 = empty slot).
+// A warp's KP largest words, spread over its lanes in descending order: lane j
+// < KP holds the j-th largest (0 = empty), lanes >= KP hold 0.  An insertion is
+// one ballot (how many held words beat the new one) and one shuffle (the words
+// below it move down a lane), so keeping the list costs the warp a few
+// instructions per word that enters, and nothing per word that does not: a
+// value filter (one comparison per logit against the value of the last word)
+// lets through a superset of the words that beat it, and the exact 64-bit
+// comparison decides.
 template <int KP>
-__device__ __forceinline__ void dt_offer(uint64_t (&l)[KP], uint64_t x) {
-    if (x <= l[KP - 1]) return;
-#pragma unroll
-    for (int i = KP - 1; i > 0; --i) l[i] = (x > l[i - 1]) ? l[i - 1] : (x > l[i] ? x : l[i]);
-    l[0] = x > l[0] ? x : l[0];
-}
+struct DtWarpList {
+    uint64_t w = 0;
+    float thr = -INFINITY;  // value of the last word once the list is full, warp-uniform
+    uint64_t last = 0;      // the last word (0 while the list is not full), warp-uniform
 
-// The KP largest words over the lists of all 32 lanes of the warp, largest
-// first; lane 0 stores them to out[0 .. KP).  Called by the whole warp.
-template <int KP>
-__device__ __forceinline__ void dt_warp_top(uint64_t (&l)[KP], uint64_t* out, int lane) {
-#pragma unroll 1
-    for (int r = 0; r < KP; ++r) {
-        const uint64_t h = l[0];
-        const uint32_t hh = (uint32_t)(h >> 32);
-        const uint32_t mh = __reduce_max_sync(0xffffffffu, hh);
-        const uint32_t ml = __reduce_max_sync(0xffffffffu, hh == mh ? (uint32_t)h : 0u);
-        const uint64_t best = ((uint64_t)mh << 32) | ml;
-        if (best != 0 && h == best) {
-#pragma unroll
-            for (int i = 0; i < KP - 1; ++i) l[i] = l[i + 1];
-            l[KP - 1] = 0;
-        }
-        if (lane == 0) out[r] = best;
+    // x is distinct from every held word; it enters when it beats the last one
+    __device__ __forceinline__ void insert(uint64_t x, int lane) {
+        const int pos = __popc(__ballot_sync(0xffffffffu, lane < KP && w > x));
+        if (pos >= KP) return;
+        const uint64_t up = __shfl_up_sync(0xffffffffu, w, 1);
+        if (lane < KP) w = (lane < pos) ? w : (lane == pos ? x : up);
+        last = __shfl_sync(0xffffffffu, w, KP - 1);
+        if (last != 0) thr = dt_unkey((uint32_t)(last >> 32));
     }
-}
+    // every lane's logit v of token id, where `has` is set; after each insertion
+    // the lanes still to come are filtered again against the raised threshold
+    __device__ __forceinline__ void offer(float v, int id, bool has, int lane) {
+        unsigned hits = __ballot_sync(0xffffffffu, has && v >= thr);
+        while (hits) {
+            const int src = __ffs(hits) - 1;
+            insert(dt_word(__shfl_sync(0xffffffffu, v, src), __shfl_sync(0xffffffffu, id, src)),
+                   lane);
+            hits &= __ballot_sync(0xffffffffu, has && v >= thr) & ~((2u << src) - 1u);
+        }
+    }
+};
 
 // (m, s) <- the pair of the union: max, and sum of exp(x - max).
 __device__ __forceinline__ void dt_combine(float& m, float& s, float m2, float s2) {
@@ -109,55 +116,157 @@ __device__ __forceinline__ void dt_warp_combine(float& m, float& s) {
     }
 }
 
-// One thread's running state over its logits, visited in increasing token order.
-// Once the list is full, a logit can enter only if its value is above the value
-// of the list's last word (an equal value has a higher token id than every
-// entry, so its word is smaller): one float comparison per logit, and the
-// 64-bit word is formed only for the few that enter.  The sum of exp uses the
-// hardware exponential (arguments <= 0; a few units in the last place for the
-// terms near the maximum, which carry the sum).
-template <int KP>
-struct DtTake {
-    float m = -INFINITY, s = 0.f;
-    float thr = -INFINITY;  // value of top[KP - 1] once the list is full
-    bool full = false;
-    bool bad = false;
-    uint64_t top[KP];
-    __device__ __forceinline__ DtTake() {
+// The k-th largest (k <= 32) of the warp's values x, by a bitonic sort of their
+// order-preserving keys (NaN keys sort as values; a NaN bound lets nothing
+// through, and a row holding NaN is reported as bad values anyway).
+__device__ __forceinline__ float dt_warp_kth(float x, int k, int lane) {
+    uint32_t key = dt_key(x);
 #pragma unroll
-        for (int i = 0; i < KP; ++i) top[i] = 0;
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
+            // descending overall: the lower lane of a pair keeps the larger key
+            // in blocks of `size` whose bit is clear, the smaller where it is set
+            const bool lower = (lane & j) == 0;
+            const bool desc = (lane & size) == 0;
+            const uint32_t hi = max(key, other), lo = min(key, other);
+            key = (lower == desc) ? hi : lo;
+        }
     }
-    __device__ __forceinline__ void offer(float a, int t) {
-        if (full && !(a > thr)) return;
-        dt_offer<KP>(top, dt_word(a, t));
-        full = top[KP - 1] != 0;
-        if (full) thr = dt_unkey((uint32_t)(top[KP - 1] >> 32));
+    return dt_unkey(__shfl_sync(0xffffffffu, key, k - 1));
+}
+
+// Descending bitonic sort of the warp's 32 words: lane i ends with the i-th largest.
+__device__ __forceinline__ uint64_t dt_sort32(uint64_t key, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool keep_hi = ((lane & j) == 0) == ((lane & size) == 0);
+            key = keep_hi ? (key > other ? key : other) : (key < other ? key : other);
+        }
     }
-    // four consecutive logits starting at token t
-    __device__ __forceinline__ void take4(float a0, float a1, float a2, float a3, int t) {
-        bad |= !(a0 < INFINITY) || !(a1 < INFINITY) || !(a2 < INFINITY) || !(a3 < INFINITY);
-        const float mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+    return key;
+}
+// Lanes 0-15 and lanes 16-31 each hold a descending run: the 32 words in
+// descending order (the upper run reversed makes one bitonic sequence, then
+// five half-cleaner stages).
+__device__ __forceinline__ uint64_t dt_merge32(uint64_t key, int lane) {
+    key = __shfl_sync(0xffffffffu, key, lane < 16 ? lane : 47 - lane);
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, key, j);
+        key = ((lane & j) == 0) ? (key > other ? key : other) : (key < other ? key : other);
+    }
+    return key;
+}
+// The 16 largest of words ld(0 .. n) (0 = none), descending in lanes 0-15 of the
+// calling warp.  The words come in runs of `run` (a power of two <= 16), each
+// descending: runs of 16 are merged into the best 16 so far, shorter runs
+// sorted together with them.  Eight loads a lane are in flight.
+template <class Load>
+__device__ __forceinline__ uint64_t dt_top16(int n, int run, int lane, Load ld) {
+    uint64_t top = 0;  // lanes 0-15: the best so far
+    for (int g0 = 0; g0 < n; g0 += 16 * 8) {
+        uint64_t nw[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = g0 + 16 * j + lane - 16;
+            nw[j] = (lane >= 16 && e < n) ? ld(e) : 0ull;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (g0 + 16 * j >= n) break;  // uniform across the warp
+            const uint64_t x = (lane < 16) ? top : nw[j];
+            top = (run == 16) ? dt_merge32(x, lane) : dt_sort32(x, lane);
+        }
+    }
+    return top;
+}
+
+// One CTA's pass over logits [lo, hi) of a row: each thread keeps a running
+// (max, sum of exp) of the logits it loads, its warp keeps the warp's KP best
+// words.  Every thread loads DT_U 16-byte vectors (4 * DT_U scalars without
+// them) before it uses any, and the block steps through the range in lock step
+// so the warp-wide list operations see converged warps.  The sum of exp uses
+// the hardware exponential (arguments <= 0; a few units in the last place for
+// the terms near the maximum, which carry the sum).
+constexpr int DT_U = 4;
+constexpr float DT_LOG2E = 1.4426950408889634f;
+
+template <int KP, bool VEC>
+__device__ __forceinline__ void dt_stream(const float* x, int lo, int hi, int tid, int lane,
+                                          DtWarpList<KP>& L, float& m, float& s, bool& bad) {
+    constexpr int E = 4 * DT_U;  // logits per thread per step
+    const int nstep = (hi - lo + E * DT_THREADS - 1) / (E * DT_THREADS);
+    for (int st = 0; st < nstep; ++st) {
+        float a[E];
+        int t0[DT_U];
+        bool in[DT_U];
+        if (VEC) {
+#pragma unroll
+            for (int u = 0; u < DT_U; ++u) {
+                const int i = lo + st * E * DT_THREADS + (u * DT_THREADS + tid) * 4;
+                t0[u] = i;
+                in[u] = i < hi;  // the chunk length is a multiple of 4
+                const float4 v = in[u] ? __ldcs(reinterpret_cast<const float4*>(x + i))
+                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                a[4 * u] = v.x;
+                a[4 * u + 1] = v.y;
+                a[4 * u + 2] = v.z;
+                a[4 * u + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < DT_U; ++u) {
+                t0[u] = lo + st * E * DT_THREADS + u * 4 * DT_THREADS + tid;
+                in[u] = true;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = t0[u] + c * DT_THREADS;
+                    a[4 * u + c] = (i < hi) ? __ldcs(x + i) : -INFINITY;
+                }
+            }
+        }
+        float mx = a[0];
+#pragma unroll
+        for (int e = 0; e < E; ++e) mx = fmaxf(mx, a[e]);  // ignores NaN
+        // first step: the KP-th largest of the lanes' maxima bounds the KP-th
+        // largest logit from below (the KP largest maxima are KP distinct
+        // logits), so nothing below it can enter; a warp sort of the maxima
+        if (st == 0) L.thr = dt_warp_kth(mx, KP, lane);
         if (mx > m) {
             s = (m == -INFINITY) ? 0.f : s * expf(m - mx);
             m = mx;
         }
-        if (m > -INFINITY)
-            s += (__expf(a0 - m) + __expf(a1 - m)) + (__expf(a2 - m) + __expf(a3 - m));
-        offer(a0, t);
-        offer(a1, t + 1);
-        offer(a2, t + 2);
-        offer(a3, t + 3);
-    }
-    __device__ __forceinline__ void take1(float a, int t) {
-        bad |= !(a < INFINITY);
-        if (a > m) {
-            s = (m == -INFINITY) ? 0.f : s * expf(m - a);
-            m = a;
+        if (m > -INFINITY) {
+            // exp(a - m) = 2^(a log2 e - m log2 e), one fma per logit; a NaN logit
+            // makes the step's sum NaN, +inf makes the maximum +inf
+            const float ml = m * DT_LOG2E;
+            float s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) s2 += ex2_approx(fmaf(a[e], DT_LOG2E, -ml));
+            s += s2;
+            bad |= !(s2 == s2) || mx == INFINITY;
+        } else {
+            // nothing finite yet: every value still needs its own NaN / +inf check
+#pragma unroll
+            for (int e = 0; e < E; ++e) bad |= !(a[e] < INFINITY);
         }
-        if (m > -INFINITY) s += __expf(a - m);
-        offer(a, t);
+        // the warp looks at the step's logits only when one of them can enter
+        if (__any_sync(0xffffffffu, mx >= L.thr)) {
+#pragma unroll
+            for (int u = 0; u < DT_U; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int id = VEC ? t0[u] + c : t0[u] + c * DT_THREADS;
+                    L.offer(a[4 * u + c], id, VEC ? in[u] : id < hi, lane);
+                }
+        }
     }
-};
+}
 
 template <int KP, bool VEC>
 __global__ void __launch_bounds__(DT_THREADS) draft_expand_kernel(DtParams p) {
@@ -175,6 +284,7 @@ __global__ void __launch_bounds__(DT_THREADS) draft_expand_kernel(DtParams p) {
     __shared__ int s_rowbad[DT_K_MAX];
     __shared__ uint64_t s_cand[DT_K_MAX * DT_K_MAX];
     __shared__ uint64_t s_next[KP];
+    __shared__ uint64_t s_fr[DT_WARPS * 16];
     __shared__ uint64_t s_sort[DT_NODES_MAX];
     __shared__ int s_kid[64], s_kdep[64], s_kpar[64], s_kpn[64], s_knew[64];
 
@@ -183,28 +293,20 @@ __global__ void __launch_bounds__(DT_THREADS) draft_expand_kernel(DtParams p) {
         const float* x = p.logits + (int64_t)row * p.V;
         const int lo = chunk * p.per;
         const int hi = min(p.V, lo + p.per);
-        DtTake<KP> acc;
-        if (VEC) {
-            for (int i = lo + 4 * tid; i < hi; i += 4 * DT_THREADS) {
-                const float4 v = __ldcs(reinterpret_cast<const float4*>(x + i));
-                acc.take4(v.x, v.y, v.z, v.w, i);
-            }
-        } else {
-            for (int i = lo + tid; i < hi; i += DT_THREADS) acc.take1(__ldcs(x + i), i);
-        }
-        const bool bad = __syncthreads_or(acc.bad ? 1 : 0) != 0;
-        float m = acc.m, s = acc.s;
+        DtWarpList<KP> L;
+        float m = -INFINITY, s = 0.f;
+        bool bad_t = false;
+        dt_stream<KP, VEC>(x, lo, hi, tid, lane, L, m, s, bad_t);
+        const bool bad = __syncthreads_or(bad_t ? 1 : 0) != 0;
         dt_warp_combine(m, s);
         if (lane == 0) s_wms[warp] = make_float2(m, s);
-        dt_warp_top<KP>(acc.top, &s_wtop[warp * KP], lane);
+        if (lane < KP) s_wtop[warp * KP + lane] = L.w;
         __syncthreads();
         if (warp == 0) {
-            uint64_t l[KP];
-#pragma unroll
-            for (int i = 0; i < KP; ++i) l[i] = 0;
-            for (int e = lane; e < DT_WARPS * KP; e += 32) dt_offer<KP>(l, s_wtop[e]);
+            // the warps' lists (descending runs of KP) into the chunk's KP best
+            const uint64_t t = dt_top16(DT_WARPS * KP, KP, lane, [&](int e) { return s_wtop[e]; });
             const int64_t slot = (int64_t)row * DT_CH_MAX + chunk;
-            dt_warp_top<KP>(l, p.top + slot * KP, lane);
+            if (lane < KP) p.top[slot * KP + lane] = t;
             float bm = (lane < DT_WARPS) ? s_wms[lane].x : -INFINITY;
             float bs = (lane < DT_WARPS) ? s_wms[lane].y : 0.f;
             dt_warp_combine(bm, bs);
@@ -265,12 +367,10 @@ __global__ void __launch_bounds__(DT_THREADS) draft_expand_kernel(DtParams p) {
             }
             dt_warp_combine(m, s);
             bad = __any_sync(0xffffffffu, bad);
-            uint64_t l[KP];
-#pragma unroll
-            for (int i = 0; i < KP; ++i) l[i] = 0;
+            // every chunk's list (descending runs of KP)
             const uint64_t* src = p.top + r * DT_CH_MAX * KP;
-            for (int e = lane; e < p.c * KP; e += 32) dt_offer<KP>(l, __ldcg(src + e));
-            dt_warp_top<KP>(l, s_rtop[f], lane);
+            const uint64_t t = dt_top16(p.c * KP, KP, lane, [&](int e) { return __ldcg(src + e); });
+            if (lane < KP) s_rtop[f][lane] = t;
             if (lane == 0) {
                 s_lse[f] = m + logf(s);
                 s_rowbad[f] = (bad || !(m > -INFINITY)) ? 1 : 0;
@@ -322,12 +422,17 @@ __global__ void __launch_bounds__(DT_THREADS) draft_expand_kernel(DtParams p) {
     }
     __syncthreads();
     // ---- next frontier: the k best new nodes, best first -----------------
+    // each warp sorts 32 candidates, then warp 0 merges the warps' best 16
+    static_assert(DT_K_MAX * DT_K_MAX <= 32 * DT_WARPS, "one sort round per warp");
+    {
+        const int e = warp * 32 + lane;
+        const uint64_t t = dt_sort32(e < nnew ? s_cand[e] : 0ull, lane);
+        if (lane < 16) s_fr[warp * 16 + lane] = t;
+    }
+    __syncthreads();
     if (warp == 0) {
-        uint64_t l[KP];
-#pragma unroll
-        for (int i = 0; i < KP; ++i) l[i] = 0;
-        for (int e = lane; e < nnew; e += 32) dt_offer<KP>(l, s_cand[e]);
-        dt_warp_top<KP>(l, s_next, lane);
+        const uint64_t t = dt_top16(DT_WARPS * 16, 16, lane, [&](int e) { return s_fr[e]; });
+        if (lane < KP) s_next[lane] = t;
     }
     __syncthreads();
     if (tid < p.k) {
@@ -462,12 +567,15 @@ int64_t draft_tree_nodes(int k, int layers) {
 size_t draft_tree_ws_bytes(int B, int k, int layers) { return dt_layout(B, k, layers).total; }
 
 // Chunks per row: enough CTAs to cover the GPU about four times, at least
-// 2048 logits per chunk, at most DT_CH_MAX chunks; `per` is the chunk length
-// (a multiple of 4 for 16-byte loads).
+// DT_CHUNK_MIN logits per chunk (every warp's list costs a few dozen
+// insertions to fill, so short chunks spend more on their lists than on the
+// stream), at most DT_CH_MAX chunks; `per` is the chunk length (a multiple of
+// 4 for 16-byte loads).
+constexpr int DT_CHUNK_MIN = 16384;
 void draft_tree_chunks(int rows, int V, bool vec, int* c_out, int* per_out) {
     const int64_t target = 4 * (int64_t)device_sm_count();
     int64_t c = (target + rows - 1) / rows;
-    c = std::min<int64_t>(c, (V + 2047) / 2048);
+    c = std::min<int64_t>(c, (V + DT_CHUNK_MIN - 1) / DT_CHUNK_MIN);
     c = std::max<int64_t>(1, std::min<int64_t>(c, DT_CH_MAX));
     int64_t per = (V + c - 1) / c;
     if (vec) per = (per + 3) / 4 * 4;

@@ -106,12 +106,13 @@ def compare(tv, orc, rows, roots, k, N, min_exact=1):
     return exact
 
 
-SMALL = [  # B, V, topk, layers, N, seed
+SMALL = [  # B, V, topk, layers, N, seed (chunks hold at least 16384 logits)
     (3, 1000, 4, 4, 20, 1),     # 16-byte loads, one chunk per row
     (2, 1001, 3, 3, 13, 2),     # odd vocabulary: scalar loads
-    (4, 5000, 8, 3, 64, 3),     # 8-entry lists, several chunks
+    (4, 50000, 8, 3, 64, 3),    # 8-entry lists, several chunks
     (2, 3000, 10, 2, 64, 4),    # 16-entry lists for k = 10
-    (2, 40000, 16, 2, 64, 5),   # k = 16, 19 chunks of 2108 logits, ragged tail
+    (2, 40000, 16, 2, 64, 5),   # k = 16, three chunks, ragged tail
+    (2, 40001, 4, 2, 16, 10),   # scalar loads over three chunks
     (2, 777, 1, 6, 7, 6),       # k = 1: the greedy chain
     (2, 500, 5, 1, 6, 7),       # one layer: expand and finish in one call
     (3, 64, 4, 3, 1, 8),        # N = 1: the root alone
