@@ -15,9 +15,6 @@ and merge kernel use the array well beyond its counters.  The calls are
 interleaved so that every call after the first starts from scratch left dirty
 by a call of another shape.
 
-This file is collected after the parity tests so that a run stopping at its
-first failure has already run them; it also passes on its own in a fresh
-process.
 """
 import numpy as np
 import pytest
