@@ -206,7 +206,9 @@ tv_status tree_verify_attention(const void* q, const void* k_cache, const void* 
  *   of the last rejected child's draw; when cur is a leaf the bonus token is
  *   drawn from target[cur] with w1 of the draw for k = N (leaf N-1) or
  *   k = N + cur.  On a chain both descriptions agree.  A tree is walked by
- *   one CTA per sequence.
+ *   one thread-block cluster per sequence, launched after the chain kernel
+ *   on the same stream (so a stochastic call launches two kernels when
+ *   N > 2).
  *
  * Outputs: accept_len int32 [B] = depth of the chosen node (number of
  * accepted drafts); path int32 [B][max_path] = node ids root..chosen, then
