@@ -882,6 +882,7 @@ accept_stochastic_tree_kernel(AccParams p) {
     __shared__ uint64_t rS[64];     // residual sum after each of those rejections
     __shared__ uint64_t tred[CH_WARPS];
     __shared__ uint64_t xpart[2];   // this slice's sum, by pass parity (read by the cluster)
+    __shared__ uint64_t gsum[CH_WARPS * TW_U];  // the draw: each warp's total of each group
     if (tid < 64) {
         spar[tid] = (tid < N && tid < Nmax) ? p.parents[(int64_t)b * Nmax + tid] : 0;
         stok[tid] = (tid < N && tid < Nmax) ? p.tokens[(int64_t)b * Nmax + tid] : 0;
@@ -1007,44 +1008,67 @@ accept_stochastic_tree_kernel(AccParams p) {
             for (int base = lo; base < hi; base += TW_TILE) {
                 uint64_t w[TW_U][4];
                 tile_weights(pc, m, base, w);
-                bool done = false;
+                // the tile's groups (group u: entries base + u * 4 * CH_THREADS onwards,
+                // four a thread) are totalled in one reduction, and only the group
+                // holding T is scanned
+                uint64_t s4[TW_U];
 #pragma unroll
                 for (int u = 0; u < TW_U; ++u) {
-                    const uint64_t s4 = (w[u][0] + w[u][1]) + (w[u][2] + w[u][3]);
-                    uint64_t incl = s4;  // inclusive scan over the warp's lanes
+                    s4[u] = (w[u][0] + w[u][1]) + (w[u][2] + w[u][3]);
+                    uint64_t v = s4[u];
 #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    __syncthreads();  // earlier readers of tred are done
-                    if (lane == 31) tred[warp] = incl;
-                    __syncthreads();
-                    uint64_t wpre = 0, tot = 0;
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) gsum[warp * TW_U + u] = v;
+                }
+                __syncthreads();
+                int gu = -1;
+                uint64_t gbase = 0;
 #pragma unroll
-                    for (int i = 0; i < CH_WARPS; ++i) {
-                        wpre += (i < warp) ? tred[i] : 0ull;
-                        tot += tred[i];
-                    }
-                    const uint64_t ex = run + wpre + (incl - s4);
-                    if (ex <= T && T - ex < s4) {  // this thread's four entries hold it
-                        uint64_t r = ex;
-                        int hit = -1;  // the first entry whose inclusive prefix exceeds T
+                for (int u = 0; u < TW_U; ++u) {
+                    uint64_t t = 0;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            r += w[u][c];
-                            if (hit < 0 && r > T) hit = c;
-                        }
-                        sfound = base + (u * CH_THREADS + tid) * 4 + hit;
+                    for (int i = 0; i < CH_WARPS; ++i) t += gsum[i * TW_U + u];
+                    if (gu < 0 && run <= T && T - run < t) {
+                        gu = u;
+                        gbase = run;
                     }
-                    run += tot;
-                    __syncthreads();
-                    if (sfound >= 0) {
-                        done = true;
-                        break;
+                    run += t;
+                }
+                __syncthreads();  // every read of gsum and tred is done
+                if (gu < 0) continue;  // uniform: T lies in a later tile
+                uint64_t e4[4] = {0ull, 0ull, 0ull, 0ull}, t4 = 0;
+#pragma unroll
+                for (int u = 0; u < TW_U; ++u) {
+                    if (u == gu) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) e4[c] = w[u][c];
+                        t4 = s4[u];
                     }
                 }
-                if (done) break;
+                uint64_t incl = t4;  // inclusive scan over the warp's lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (lane == 31) tred[warp] = incl;
+                __syncthreads();
+                uint64_t wpre = 0;
+#pragma unroll
+                for (int i = 0; i < CH_WARPS; ++i) wpre += (i < warp) ? tred[i] : 0ull;
+                const uint64_t ex = gbase + wpre + (incl - t4);
+                if (ex <= T && T - ex < t4) {  // this thread's four entries hold it
+                    uint64_t r = ex;
+                    int hit = -1;  // the first entry whose inclusive prefix exceeds T
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        r += e4[c];
+                        if (hit < 0 && r > T) hit = c;
+                    }
+                    sfound = base + (gu * CH_THREADS + tid) * 4 + hit;
+                }
+                __syncthreads();
+                break;  // uniform
             }
             if (tid == 0) *cluster.map_shared_rank(&xtok, 0) = sfound;
         }
